@@ -1,0 +1,228 @@
+"""Checks that pin the float64 oracle to facts outside itself.
+
+Each check takes an implementation namespace ``impl`` exposing
+``forward_head(q, k, v, scale, causal) -> (O, L)``,
+``backward_head(q, k, v, dO, scale, causal) -> (dQ, dK, dV, D)`` and
+``online_softmax_row``; the real oracle passes every check
+(test_oracle_pins.py) and each deliberately broken copy of it fails at least
+one (test_oracle_mutants.py).  None of the checks re-types the attention
+formula: they use closed forms, a library routine (torch SDPA / autograd and
+scipy logsumexp, both in float64 on the CPU), finite differences, or
+invariants the mathematics fixes.
+"""
+
+import math
+import os
+
+import numpy as np
+import torch
+from scipy.special import logsumexp
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def load_split_tile_example():
+    scores, tiles = None, []
+    with open(os.path.join(GOLDEN, "split_tile_softmax.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            if key == "scores":
+                scores = [float(x) for x in vals]
+            elif key == "tile":
+                tiles.append((int(vals[0]), int(vals[1])))
+    return scores, tiles
+
+
+# ---------------------------------------------------------------- worked example
+
+def check_split_tile_example(impl):
+    """tensortonic.com "FlashAttention" sections 4-5: scores [1,2,3,4] in tiles
+    [1,2] and [3,4]; the merged running state must equal the full-row softmax."""
+    scores, tiles = load_split_tile_example()
+    assert scores == [1.0, 2.0, 3.0, 4.0] and tiles == [(0, 2), (2, 4)]
+    e = [math.exp(s) for s in scores]
+    weights = [x / sum(e) for x in e]
+    lse = math.log(sum(e))
+    # running state after each tile, in closed form
+    m1, l1 = 2.0, math.exp(-1.0) + 1.0
+    m2, l2 = 4.0, l1 * math.exp(2.0 - 4.0) + math.exp(-1.0) + 1.0
+    out, L, states = impl.online_softmax_row(scores, np.eye(4), tiles)
+    np.testing.assert_allclose(out, weights, rtol=0, atol=1e-15)
+    assert abs(L - lse) < 1e-14
+    assert abs(states[0][0] - m1) == 0 and abs(states[0][1] - l1) < 1e-15
+    assert abs(states[1][0] - m2) == 0 and abs(states[1][1] - l2) < 1e-15
+    # the same numbers through the full attention definition: one query whose
+    # dot products with four keys are 1, 2, 3, 4 and one-hot values
+    O, Lf = impl.forward_head(np.array([[1.0]]), np.array([[1.0], [2.0], [3.0], [4.0]]),
+                              np.eye(4), 1.0, False)
+    np.testing.assert_allclose(O[0], weights, rtol=0, atol=1e-15)
+    assert abs(Lf[0] - lse) < 1e-14
+    # the page's point: softmax per tile gives each tile a full unit of weight
+    per_tile = sum(sum(math.exp(s) for s in scores[a:b]) / sum(math.exp(s) for s in scores[a:b])
+                   for a, b in tiles)
+    assert abs(per_tile - 2.0) < 1e-15
+
+
+# ---------------------------------------------------------------- closed forms
+
+def check_zero_query(impl):
+    """Q = 0 makes every allowed score 0: uniform weights.  Non-causal
+    O_i = mean(V), L_i = log n; causal O_i = mean(V[:i+1]), L_i = log(i+1)."""
+    r = _rng(11)
+    n, d = 9, 5
+    q = np.zeros((n, d))
+    k = r.standard_normal((n, d))
+    v = r.standard_normal((n, d))
+    O, L = impl.forward_head(q, k, v, 0.37, False)
+    np.testing.assert_allclose(O, np.broadcast_to(v.mean(0), (n, d)), atol=1e-14)
+    np.testing.assert_allclose(L, np.full(n, math.log(n)), atol=1e-14)
+    O, L = impl.forward_head(q, k, v, 0.37, True)
+    running_mean = np.cumsum(v, 0) / np.arange(1, n + 1)[:, None]
+    np.testing.assert_allclose(O, running_mean, atol=1e-14)
+    np.testing.assert_allclose(L, np.log(np.arange(1, n + 1)), atol=1e-14)
+
+
+def check_one_hot(impl):
+    """Orthogonal keys and q_i = c k_i with large c: weight ~1 on key i, so
+    O = V (error ~ n exp(-c^2)) and L = c^2 up to the same error."""
+    n = 6
+    c = 8.0
+    k = np.eye(n)
+    q = c * np.eye(n)
+    v = _rng(12).standard_normal((n, 3))
+    O, L = impl.forward_head(q, c * k, v, 1.0, False)
+    # off-diagonal weights are exp(-64) ~ 1.6e-28, far below float64 rounding
+    np.testing.assert_allclose(O, v, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L, np.full(n, c * c), rtol=0, atol=1e-13)
+
+
+def check_rows_sum_to_one(impl):
+    """tensortonic.com "FlashAttention" section 1: the weights of a row sum to
+    one, so V = 1 gives O = 1 and V + c gives O + c."""
+    r = _rng(13)
+    n, d = 11, 4
+    q, k, v = r.standard_normal((3, n, d))
+    for causal in (False, True):
+        O1, _ = impl.forward_head(q, k, np.ones((n, d)), 0.5, causal)
+        np.testing.assert_allclose(O1, 1.0, atol=1e-14)
+        O, _ = impl.forward_head(q, k, v, 0.5, causal)
+        Oc, _ = impl.forward_head(q, k, v + 2.5, 0.5, causal)
+        np.testing.assert_allclose(Oc, O + 2.5, atol=1e-13)
+
+
+def check_causal_future_blind(impl):
+    """tensortonic.com "FlashAttention" sections 1 and 6: a causal row never
+    reads a later key; row 0 reads only key 0 (O_0 = V_0, L_0 = s_00)."""
+    r = _rng(14)
+    n, d = 10, 4
+    q, k, v = r.standard_normal((3, n, d))
+    O, L = impl.forward_head(q, k, v, 0.7, True)
+    np.testing.assert_allclose(O[0], v[0], atol=1e-15)
+    assert abs(L[0] - 0.7 * float(q[0] @ k[0])) < 1e-14
+    for i in range(n - 1):
+        k2, v2 = k.copy(), v.copy()
+        k2[i + 1:] = r.standard_normal((n - i - 1, d)) * 3
+        v2[i + 1:] = r.standard_normal((n - i - 1, d)) * 3
+        O2, L2 = impl.forward_head(q, k2, v2, 0.7, True)
+        np.testing.assert_allclose(O2[:i + 1], O[:i + 1], atol=1e-14)
+        np.testing.assert_allclose(L2[:i + 1], L[:i + 1], atol=1e-14)
+        assert np.abs(O2[i + 1:] - O[i + 1:]).max() > 1e-3   # later rows do see them
+
+
+def check_logsumexp_library(impl):
+    """L_i is the logarithm of the full row's exponential sum (tensortonic.com
+    "FlashAttention" section 7) -- compared with scipy's logsumexp over the
+    allowed entries of the row."""
+    r = _rng(15)
+    n, d = 13, 6
+    q, k, v = r.standard_normal((3, n, d)) * 2.0
+    for causal in (False, True):
+        _, L = impl.forward_head(q, k, v, 0.3, causal)
+        for i in range(n):
+            lim = i + 1 if causal else n
+            row = [0.3 * float(np.dot(q[i], k[j])) for j in range(lim)]
+            assert abs(L[i] - logsumexp(row)) < 1e-12
+
+
+def _torch_reference(q, k, v, do, scale, causal):
+    """torch's scaled_dot_product_attention (float64 math path on the CPU)
+    with autograd: a library routine independent of the oracle."""
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq[None, None], tk[None, None], tv[None, None], is_causal=causal, scale=scale)[0, 0]
+    out.backward(torch.tensor(do, dtype=torch.float64))
+    return (out.detach().numpy(), tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy())
+
+
+def check_torch_sdpa(impl):
+    """Forward and gradients against torch SDPA + autograd in float64."""
+    r = _rng(16)
+    for n, d, causal in ((7, 3, False), (7, 3, True), (33, 8, True), (20, 16, False)):
+        q, k, v, do = r.standard_normal((4, n, d))
+        scale = 1.0 / math.sqrt(d)
+        O, _ = impl.forward_head(q, k, v, scale, causal)
+        dQ, dK, dV, _ = impl.backward_head(q, k, v, do, scale, causal)
+        tO, tdq, tdk, tdv = _torch_reference(q, k, v, do, scale, causal)
+        np.testing.assert_allclose(O, tO, atol=1e-12)
+        np.testing.assert_allclose(dQ, tdq, atol=1e-12)
+        np.testing.assert_allclose(dK, tdk, atol=1e-12)
+        np.testing.assert_allclose(dV, tdv, atol=1e-12)
+
+
+def check_finite_differences(impl):
+    """Central differences (h = 1e-6) of the scalar loss <dO, O> against the
+    analytic gradients, n = 6, d = 4, causal and not."""
+    r = _rng(17)
+    n, d, h = 6, 4, 1e-6
+    q, k, v, do = r.standard_normal((4, n, d))
+    for causal in (False, True):
+        dQ, dK, dV, _ = impl.backward_head(q, k, v, do, 0.45, causal)
+
+        def loss(qq, kk, vv):
+            return float((impl.forward_head(qq, kk, vv, 0.45, causal)[0] * do).sum())
+
+        for which, grad in ((0, dQ), (1, dK), (2, dV)):
+            fd = np.zeros((n, d))
+            for i in range(n):
+                for j in range(d):
+                    args_p = [q.copy(), k.copy(), v.copy()]
+                    args_m = [q.copy(), k.copy(), v.copy()]
+                    args_p[which][i, j] += h
+                    args_m[which][i, j] -= h
+                    fd[i, j] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            np.testing.assert_allclose(grad, fd, atol=2e-8, rtol=1e-6)
+
+
+def check_gradient_invariants(impl):
+    """Each row of dS sums to zero (softmax Jacobian), so sum_j dK_j = 0; each
+    row of P sums to one, so sum_j dV_j = sum_i dO_i; and D_i = sum_j P_ij dP_ij
+    equals rowsum(dO o O)."""
+    r = _rng(18)
+    n, d = 12, 5
+    q, k, v, do = r.standard_normal((4, n, d))
+    for causal in (False, True):
+        dQ, dK, dV, D = impl.backward_head(q, k, v, do, 0.6, causal)
+        np.testing.assert_allclose(dK.sum(0), 0.0, atol=1e-13)
+        np.testing.assert_allclose(dV.sum(0), do.sum(0), atol=1e-13)
+        O, _ = impl.forward_head(q, k, v, 0.6, causal)
+        np.testing.assert_allclose(D, (do * O).sum(1), atol=1e-13)
+
+
+ALL_CHECKS = [
+    check_split_tile_example,
+    check_zero_query,
+    check_one_hot,
+    check_rows_sum_to_one,
+    check_causal_future_blind,
+    check_logsumexp_library,
+    check_torch_sdpa,
+    check_finite_differences,
+    check_gradient_invariants,
+]
