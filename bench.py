@@ -1,0 +1,366 @@
+"""Throughput of exact attention, forward + backward, on GB300.
+
+One step = fa_fwd then fa_bwd over one batch of seeded synthetic bf16 input
+of the causal B=2 H=32 N=4096 D=128 workload (the seq-4096, 32-head shape of
+the pages' timing example), inputs resident in device memory.  Prints ONE
+JSON line (rank 0).  ``value`` is fwd+bwd TFLOP/s with FLOPs counted as
+4*B*H*N^2*D (halved when causal) for the forward pass and 2.5x that for the
+backward pass; ``fwd_tflops`` is the forward pass alone.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica (the path has no exchange
+step), the timed region is bracketed by barriers and the slowest rank's time
+is reported.  ``--impl reference`` times the float64 CPU oracle on a bounded
+sample of the same workload (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "long_b2h32n4096d128"
+CAUSAL = True
+METRIC = "attention fwd & fwd+bwd TFLOP/s (bf16, causal) and % of GB300 BF16 tensor peak"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAK_TFLOPS = 1900.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel from one ncu capture, keyed by the SHA-256 of that kernel's source
+# file at capture time (reported as null once the source has changed).
+TRAFFIC_BY_SOURCE = {}
+
+
+def flops_fwd(B, H, N, D, causal):
+    f = 4.0 * B * H * N * N * D
+    return f / 2 if causal else f
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    return FALLBACK_PEAK_TFLOPS, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def kernel_source_sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def cpu_oracle_sample(q, k, v, do, scale, causal, budget_s=12.0, max_heads=None):
+    """Time the float64 oracle (forward + backward) head by head until
+    ``budget_s`` has passed.  Returns (TFLOP/s, heads done, seconds)."""
+    import oracle
+    B, H, N, D = q.shape
+    heads = [(b, h) for b in range(B) for h in range(H)][:max_heads]
+    done, t0 = 0, time.perf_counter()
+    for b, h in heads:
+        qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
+        oracle.forward_head(qn, kn, vn, scale, causal)
+        oracle.backward_head(qn, kn, vn, don, scale, causal)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 3.5 * flops_fwd(1, done, N, D, causal)
+    return flops / dt / 1e12, done, dt
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: each step is the oracle's forward +
+    backward on one head of the workload, on the host cores."""
+    if rank != 0:
+        return
+    from exact_io_aware_37_gb300 import synth
+    cfg = synth.WORKLOADS[WORKLOAD]
+    q, k, v, do = synth.make_dense(cfg)
+    B, H, N, D = q.shape
+    scale = 1.0 / D ** 0.5
+    import oracle
+    qn, kn, vn, don = (x[0, 0].double().numpy() for x in (q, k, v, do))
+    for _ in range(args.warmup):
+        oracle.forward_head(qn, kn, vn, scale, CAUSAL)
+        oracle.backward_head(qn, kn, vn, don, scale, CAUSAL)
+    times = []
+    for s in range(args.steps):
+        b, h = divmod(s % (B * H), H)
+        qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
+        t0 = time.perf_counter()
+        oracle.forward_head(qn, kn, vn, scale, CAUSAL)
+        oracle.backward_head(qn, kn, vn, don, scale, CAUSAL)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    flops = 3.5 * flops_fwd(1, 1, N, D, CAUSAL) * args.steps
+    value = flops / total / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} causal (one head per step)", "B": 1, "H": 1, "N": N, "D": D,
+                   "causal": CAUSAL},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one (b,h) head of {WORKLOAD} per step, float64 numpy fwd+bwd"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank)
+        barrier(dist)
+        return
+
+    import exact_io_aware_37_gb300 as fa
+    from exact_io_aware_37_gb300 import synth
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    cfg = synth.WORKLOADS[WORKLOAD]
+    q_h, k_h, v_h, do_h = synth.make_dense(cfg)
+    B, H, N, D = q_h.shape
+    scale = 1.0 / D ** 0.5
+    q, k, v, do = (x.to(device) for x in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(q), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches0 = fa.fa_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier(dist)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
+            ev[s][1].record(stream)
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+            ev[s][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    launches = fa.fa_launch_count() - launches0
+    assert fa.fa_get_last_device_error() == 0
+    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), device)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+
+    f_fwd = flops_fwd(B, H, N, D, CAUSAL)
+    f_step = 3.5 * f_fwd
+    ms_per_step = total_ms / args.steps
+    value = world * f_step / (ms_per_step * 1e-3) / 1e12
+    fwd_tflops = f_fwd / (statistics.mean(fwd_ms) * 1e-3) / 1e12
+    bwd_tflops = 2.5 * f_fwd / (statistics.mean(bwd_ms) * 1e-3) / 1e12
+    peak_tf, _, peak_kind = peaks()
+    path = fa.fa_path_name(torch.bfloat16, D)
+
+    # dominant kernel: the backward pass (2.5x the forward FLOPs)
+    dom_ms = statistics.mean(bwd_ms)
+    dom_name = "fa_bwd (preprocess + main kernels)"
+    src = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc",
+                       "fa_tc_bwd.cu" if path == "tcgen05" else "fa_simt.cu")
+    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src))
+    achieved = 2.5 * f_fwd / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": traffic, "kernel": dom_name,
+                "peak_kind": f"bf16 dense burst, {peak_kind}"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} causal", "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
+                   "kernel_path": path,
+                   "l2": f"inputs {4 * q.numel() * 2 / 2**20:.0f} MiB > 129 MiB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        "fwd_frac_of_peak": fwd_tflops / peak_tf, "fwdbwd_frac_of_peak": value / world / peak_tf,
+        "ms_fwd": statistics.mean(fwd_ms), "ms_bwd": statistics.mean(bwd_ms),
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, args)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, heads, secs = cpu_oracle_sample(q_h, k_h, v_h, do_h, scale, CAUSAL)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{heads} of {B * H} (b,h) heads of {WORKLOAD} causal, float64 "
+                                          f"numpy fwd+bwd, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, args):
+    """Same metric through the public API with host buffers: every step copies
+    q, k, v, dO from pinned host memory, runs fa_fwd + fa_bwd and copies o,
+    lse, dq, dk, dv back, all inside the timed region."""
+    hin = [x.pin_memory() for x in (q_h, k_h, v_h, do_h)]
+    dins = [torch.empty_like(x, device=device) for x in hin]
+    B, H, N, D = q_h.shape
+    o = torch.empty_like(dins[0])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    dq, dk, dv = (torch.empty_like(dins[0]) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_size(dins[0]), dtype=torch.uint8, device=device)
+    outs_d = [o, lse, dq, dk, dv]
+    outs_h = [torch.empty_like(x, device="cpu").pin_memory() for x in outs_d]
+
+    def step():
+        for hsrc, ddst in zip(hin, dins):
+            ddst.copy_(hsrc, non_blocking=True)
+        q, k, v, do = dins
+        fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+        for dsrc, hdst in zip(outs_d, outs_h):
+            hdst.copy_(dsrc, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    barrier(dist)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(dist, a.elapsed_time(b), device) / steps
+    f_step = 3.5 * flops_fwd(B, H, N, D, CAUSAL)
+    return {"value": world * f_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin),
+            "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in outs_h),
+            "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,137 @@
-"""Exact IO-aware tiled attention for GB300 (sm_103a)."""
+"""Exact IO-aware tiled attention for GB300 (sm_103a).
+
+Python binding of the C ABI in include/fa.h.  Functions with the C names
+(``fa_fwd``, ``fa_bwd``, ``fa_bwd_workspace_size``, ``fa_get_last_device_error``,
+``fa_strerror``, ...) marshal torch tensors to pointers and call the library;
+``forward`` / ``backward`` also allocate the outputs.  Every step of the
+computation runs in the library's CUDA kernels: torch only provides device
+memory and the current stream.
+
+Layouts: dense tensors are [B, H, N, D]; packed variable-length batches are
+[H, T, D] with int32 ``cu_seqlens`` [B + 1] on the device and ``max_seqlen``.
+"""
+
+import math
+
+import torch
+
+from ._lib import FA_BF16, FA_F32, FAError, lib, library_path  # noqa: F401
+
+__all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
+           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "forward", "backward",
+           "FAError"]
+
+_DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dims(q, cu_seqlens, max_seqlen):
+    """(B, H, N, D, T) from the tensor shapes."""
+    if cu_seqlens is None:
+        if q.dim() != 4:
+            raise ValueError("dense tensors must be [B, H, N, D]")
+        B, H, N, D = q.shape
+        return B, H, N, D, 0
+    if q.dim() != 3:
+        raise ValueError("packed tensors must be [H, T, D]")
+    if max_seqlen is None:
+        raise ValueError("packed input needs max_seqlen")
+    if cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    H, T, D = q.shape
+    return cu_seqlens.numel() - 1, H, int(max_seqlen), D, T
+
+
+def _check(*tensors):
+    ref = tensors[0]
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.device != ref.device:
+            raise ValueError("tensors must be on one device")
+
+
+def fa_strerror(status):
+    return lib().fa_strerror(int(status)).decode()
+
+
+def fa_path_name(dtype, D):
+    r = lib().fa_path_name(_DT[dtype] if isinstance(dtype, torch.dtype) else int(dtype), int(D))
+    return None if r is None else r.decode()
+
+
+def fa_launch_count():
+    return int(lib().fa_launch_count())
+
+
+def fa_set_wait_limit_ns(limit_ns):
+    lib().fa_set_wait_limit_ns(int(limit_ns))
+
+
+def fa_get_last_device_error(stream=None):
+    return lib().fa_get_last_device_error(_stream(stream))
+
+
+def fa_selftest_wait_timeout(stream=None):
+    return lib().fa_selftest_wait_timeout(_stream(stream))
+
+
+def fa_fwd(q, k, v, o, lse, causal, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):
+    """Enqueue the forward kernel: writes o (dtype of q) and lse (float32)."""
+    _check(q, k, v, o, lse, cu_seqlens)
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    st = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, scale, int(bool(causal)),
+                      _ptr(cu_seqlens), T, _DT[q.dtype], _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_fwd")
+
+
+def fa_bwd_workspace_size(q, cu_seqlens=None, max_seqlen=None):
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    return int(lib().fa_bwd_workspace_size(B, H, N, D, _ptr(cu_seqlens), T, _DT[q.dtype]))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_seqlens=None, max_seqlen=None,
+           workspace=None, stream=None):
+    """Enqueue the backward kernels: writes dq, dk, dv (dtype of q)."""
+    _check(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens)
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = fa_bwd_workspace_size(q, cu_seqlens, max_seqlen)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                      B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T, _DT[q.dtype],
+                      _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_bwd")
+
+
+def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):
+    """(o, lse) for dense [B,H,N,D] or packed [H,T,D] inputs."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, cu_seqlens, max_seqlen, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqlens=None, max_seqlen=None,
+             workspace=None, stream=None):
+    """(dq, dk, dv) given the forward outputs and the upstream gradient."""
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale, cu_seqlens, max_seqlen, workspace, stream)
+    return dq, dk, dv

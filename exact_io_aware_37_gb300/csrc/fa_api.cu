@@ -1,0 +1,214 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, the
+// per-device status word, workspace carving and kernel dispatch.
+#include <math.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "fa_internal.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+// Kernels latch failures here; read and cleared by fa_get_last_device_error.
+__device__ unsigned g_status_word;
+
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<unsigned long long> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+// Device address of this device's status word (looked up once per device,
+// with that device current).
+cudaError_t status_word(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The tensor-core kernels cover bf16 with D in {64, 128}.
+constexpr bool kHaveTcFwd = false;
+constexpr bool kHaveTcBwd = false;
+bool use_tensor_cores(fa_dtype dt, int D) { return dt == FA_BF16 && (D == 64 || D == 128); }
+
+fa_status validate(int B, int H, int N, int D, float scale, int causal, const int32_t* cu, int T, fa_dtype dt) {
+  if (B < 0 || H < 0 || N < 0 || D <= 0) return FA_ERR_INVALID;
+  if (!isfinite(scale)) return FA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+  if (dt != FA_BF16 && dt != FA_F32) return FA_ERR_UNSUPPORTED;
+  if (fa_path_name(dt, D) == nullptr) return FA_ERR_UNSUPPORTED;
+  if (cu != nullptr && T < 0) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+long long row_count(int B, int H, int N, const int32_t* cu, int T) {
+  return cu ? (long long)H * T : (long long)B * H * N;
+}
+
+bool no_work(int B, int H, int N, const int32_t* cu, int T) {
+  return B == 0 || H == 0 || N == 0 || (cu != nullptr && T == 0);
+}
+
+fa_status check_tensor(const void* p) {
+  if (p == nullptr) return FA_ERR_INVALID;
+  if (!aligned(p, 16)) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+void note_launches(unsigned n) { g_launches.fetch_add(n); }
+
+// Failure-detection self-test kernel: waits on a barrier nobody signals.
+__global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  ptx::WaitCtx w{&abort_flag, status, limit_ns};
+  ptx::mbar_wait(&bar, 0, w);  // returns false once the limit passes
+  __syncthreads();
+}
+
+cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_strerror(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported dtype or head width";
+    case FA_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA call failed";
+    case FA_ERR_TIMEOUT: return "a bounded wait inside a kernel expired";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+const char* fa_path_name(fa_dtype dt, int D) {
+  if (dt == FA_BF16 && (D == 64 || D == 128)) return kHaveTcFwd ? "tcgen05" : "simt_bf16";
+  if (dt == FA_F32 && (D == 32 || D == 64 || D == 128)) return "simt_f32";
+  return nullptr;
+}
+
+unsigned long long fa_launch_count(void) { return g_launches.load(); }
+
+void fa_set_wait_limit_ns(unsigned long long limit_ns) {
+  g_wait_limit_ns.store(limit_ns < 1000ull ? 1000ull : limit_ns);
+}
+
+fa_status fa_get_last_device_error(void* stream) {
+  unsigned* word = nullptr;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  if (status_word(&word) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const unsigned zero = 0;
+  if (v != 0 && cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  if (v & kDevTimeout) return FA_ERR_TIMEOUT;
+  if (v & kDevBadSeqlens) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(void* stream) {
+  unsigned* word = nullptr;
+  if (status_word(&word) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_wait_selftest(word, g_wait_limit_ns.load(), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return fa_get_last_device_error(stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int D, const int32_t* cu, int T, fa_dtype dt) {
+  if (B < 0 || H < 0 || N < 0 || D <= 0 || (cu && T < 0)) return 0;
+  const long long rows = row_count(B, H, N, cu, T);
+  size_t bytes = round_up((size_t)rows * sizeof(float), 256);
+  if (use_tensor_cores(dt, D)) bytes += round_up((size_t)rows * D * sizeof(float), 256);
+  return bytes;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                 float scale, int causal, const int32_t* cu, int T, fa_dtype dt, void* stream) {
+  fa_status st = validate(B, H, N, D, scale, causal, cu, T, dt);
+  if (st != FA_OK) return st;
+  if (no_work(B, H, N, cu, T)) return FA_OK;
+  for (const void* p : {q, k, v, (const void*)o})
+    if ((st = check_tensor(p)) != FA_OK) return st;
+  if (lse == nullptr) return FA_ERR_INVALID;
+  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  if (cu != nullptr && !aligned(cu, 4)) return FA_ERR_ALIGN;
+
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
+  p.scale = scale; p.causal = causal; p.cu = cu;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  if (status_word(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (kHaveTcFwd && use_tensor_cores(dt, D)) ? launch_tc_fwd(p, s) : launch_simt_fwd(p, dt, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal,
+                 const int32_t* cu, int T, fa_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = validate(B, H, N, D, scale, causal, cu, T, dt);
+  if (st != FA_OK) return st;
+  if (no_work(B, H, N, cu, T)) return FA_OK;
+  for (const void* p : {q, k, v, o, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+    if ((st = check_tensor(p)) != FA_OK) return st;
+  if (lse == nullptr) return FA_ERR_INVALID;
+  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  if (cu != nullptr && !aligned(cu, 4)) return FA_ERR_ALIGN;
+  const size_t need = fa_bwd_workspace_size(B, H, N, D, cu, T, dt);
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
+  p.dout = dout; p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
+  p.scale = scale; p.causal = causal; p.cu = cu;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  const long long rows = p.rows();
+  p.dvec = static_cast<float*>(workspace);
+  p.dq_acc = use_tensor_cores(dt, D)
+                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)rows * 4, 256))
+                 : nullptr;
+  if (status_word(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_preprocess(p, dt, p.dq_acc != nullptr, s);
+  if (e == cudaSuccess) e = (kHaveTcBwd && use_tensor_cores(dt, D)) ? launch_tc_bwd(p, s) : launch_simt_bwd(p, dt, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa.h"
+
+namespace fa {
+
+// Bits latched in the per-device status word by kernels.
+enum : unsigned {
+  kDevTimeout = 1u,     // a bounded wait ran out
+  kDevBadSeqlens = 2u,  // cu_seqlens violated its contract
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// One attention problem as the kernels see it.  Dense tensors are
+// [B, H, N, D]; packed ones are [H, T, D] split by cu_seqlens.  Either way a
+// (sequence b, head h) pair owns `len` consecutive rows starting at row
+// `base` of a row-major [rows, D] matrix, and lse/D vectors are indexed by
+// the same row number.
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dvec;      // D_i workspace (backward)
+  float* dq_acc;    // float32 dQ accumulator (backward, tensor-core path)
+  int B, H, N, D;
+  int T;            // packed token count (0 when dense)
+  float scale;
+  int causal;
+  const int32_t* cu;  // device pointer or nullptr
+  unsigned* status;   // device status word
+  unsigned long long wait_limit_ns;
+  long long rows() const { return cu ? (long long)H * T : (long long)B * H * N; }
+};
+
+// Row range owned by (b, h); false (and a latched error) on bad cu_seqlens.
+__device__ __forceinline__ bool seq_range(const Problem& p, int b, int h, long long& base, int& len) {
+  if (p.cu == nullptr) {
+    base = ((long long)b * p.H + h) * p.N;
+    len = p.N;
+    return true;
+  }
+  const int s0 = p.cu[b], s1 = p.cu[b + 1];
+  if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
+    atomicOr(p.status, kDevBadSeqlens);
+    return false;
+  }
+  base = (long long)h * p.T + s0;
+  len = s1 - s0;
+  return true;
+}
+
+__device__ __forceinline__ float ld_elem(const float* p, long long i) { return p[i]; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_elem(float* p, long long i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, long long i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+// Counts kernel launches (read by fa_launch_count); every launcher bumps it.
+void note_launches(unsigned n);
+
+// ---- launchers (defined in the kernel translation units) -------------------
+cudaError_t launch_simt_fwd(const Problem& p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_simt_bwd(const Problem& p, fa_dtype dt, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const Problem& p, fa_dtype dt, bool zero_dq_acc, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, cudaStream_t s);
+
+// tensor-core path (bf16, D in {64, 128})
+cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s);
+cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s);
+
+}  // namespace fa

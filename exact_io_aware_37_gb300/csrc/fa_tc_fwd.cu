@@ -1,0 +1,400 @@
+// Tensor-core forward kernel for sm_103a (bf16 in, fp32 accumulate).
+//
+// The method is the query-first tiled schedule of tensortonic.com
+// "FlashAttention" section 6 with the running softmax of section 5: a CTA
+// owns two 128-row query tiles of one (sequence, head), loads them once, and
+// visits the allowed 128-key K/V tiles in turn.  The score tile and the
+// output accumulator never leave the SM: S = Q K^T and u += P V are tcgen05
+// MMAs whose accumulators live in tensor memory (TMEM), and only O = u / l and
+// L = m + log(l) are written to device memory (section 7).
+//
+// Warp roles (10 warps):
+//   warps 0-3  softmax for query tile 0, warps 4-7 for query tile 1: one
+//              thread per query row (its TMEM lane), so row max and row sum
+//              are thread-local; exp2 of scores pre-scaled by scale*log2(e);
+//              P is rounded to bf16 and written back into the score columns.
+//              The same threads rescale their accumulator row when the
+//              running maximum grows by more than 2^8 (a lazy rescale: the
+//              final u / l uses the same reference maximum, so it is exact),
+//              and run the epilogue.
+//   warp 8     TMA producer: Q tiles once, then K_j / V_j into a ring of
+//              shared-memory stages (mbarrier full/empty pairs).
+//   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T, then, once the
+//              softmax of tile t has produced P_t, O_t += P_t V_j, then the
+//              next S_t.  The two query tiles alternate so the tensor core
+//              works on one tile while the other tile's softmax runs.
+// Causal: key tiles wholly in the future of a query tile are never loaded;
+// the diagonal tile (and the ragged last tile of a sequence) gets an
+// element-wise mask (section 6).  Packed variable-length batches use the
+// same kernel with per-sequence row ranges from cu_seqlens.
+//
+// TMEM columns (512 allocated): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [384,384+D); P_t (bf16 pairs) overwrites S_t columns [0,64).
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "fa_tmap.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;              // query rows per tile
+constexpr int kBN = 128;              // keys per tile
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+struct FwdParams {
+  CUtensorMap tq, tk, tv;
+  __nv_bfloat16* o;
+  float* lse;
+  const int32_t* cu;
+  unsigned* status;
+  unsigned long long limit_ns;
+  int B, H, N, T;
+  float c2;  // scale * log2(e)
+  int causal;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kTileBytes = kBM * D * 2;  // one Q, K or V tile
+  static constexpr int kHalves = D / 64;          // 64-column (128-byte) swizzle blocks
+  static constexpr int kHalfBytes = kBM * 128;    // 16 KB
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int D>
+__global__ void __maxnreg__(200) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ __align__(8) uint64_t bar_q, bar_done;
+  __shared__ __align__(8) uint64_t bar_k[C::kStages], bar_v[C::kStages], bar_free[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s[2], bar_p[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+
+  // ---- the (sequence, head) this CTA works on
+  int len, row0, slab;
+  long long out_base;
+  if (p.cu != nullptr) {
+    const int s0 = p.cu[b], s1 = p.cu[b + 1];
+    if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
+      if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
+      return;
+    }
+    len = s1 - s0;
+    row0 = s0;
+    slab = h;
+    out_base = (long long)h * p.T + s0;
+  } else {
+    len = p.N;
+    row0 = 0;
+    slab = b * p.H + h;
+    out_base = (long long)slab * p.N;
+  }
+  const int n_qt = (len + kBM - 1) / kBM;
+  const int n_pairs = (n_qt + 1) / 2;
+  // causal: the last query tiles see the most keys, so they are scheduled first
+  const int pair = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  if (pair >= n_pairs) return;
+  const int qt0 = 2 * pair;
+  const int n_kv = (len + kBN - 1) / kBN;
+  int nkv[2];
+  nkv[0] = p.causal ? min(qt0 + 1, n_kv) : n_kv;
+  nkv[1] = (qt0 + 1 < n_qt) ? (p.causal ? min(qt0 + 2, n_kv) : n_kv) : 0;
+  const int nmax = max(nkv[0], nkv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_done, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_k[s], 1);
+      mbar_init(&bar_v[s], 1);
+      mbar_init(&bar_free[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 4);  // one arrival per softmax warp
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const WaitCtx w{&abort_flag, p.status, p.limit_ns};
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tq);
+      tma_prefetch_desc(&p.tk);
+      tma_prefetch_desc(&p.tv);
+      const int nq = nkv[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bar_q, nq * C::kTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
+                      row0 + (qt0 + t) * kBM, slab);
+      int issued = 0;
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::kStages, round = j / C::kStages;
+        if (round > 0 && !mbar_wait(&bar_free[s], (round - 1) & 1, w)) break;
+        mbar_arrive_expect_tx(&bar_k[s], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_k[s], hf * 64,
+                      row0 + j * kBN, slab);
+        mbar_arrive_expect_tx(&bar_v[s], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_v[s], hf * 64,
+                      row0 + j * kBN, slab);
+        issued = j + 1;
+      }
+      if (abort_flag) {
+        // let copies already in flight land before the CTA's memory is released
+        mbar_wait_drain(&bar_q, 0, p.limit_ns);
+        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+          mbar_wait_drain(&bar_k[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
+          mbar_wait_drain(&bar_v[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(kBM, kBN, false, false);
+      const uint32_t id_o = idesc_bf16(kBM, D, false, true);
+      const uint32_t sq = smem_u32(smem + C::kQOff);
+      const uint32_t sk = smem_u32(smem + C::kKOff);
+      const uint32_t sv = smem_u32(smem + C::kVOff);
+      // S_t = Q_t K^T (both K-major): D/16 MMAs of K = 16
+      auto issue_s = [&](int t, int s) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * C::kHalfBytes + (ks & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sk + s * C::kTileBytes + off, 16, 1024);
+          mma_ss(tmem + t * 128, ad, bd, id_s, ks > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V (P from TMEM, V MN-major): 8 MMAs of K = 16 keys
+      auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t bd = sdesc_sw128(sv + s * C::kTileBytes + ks * 2048, C::kHalfBytes, 1024);
+          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, id_o, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&bar_q, 0, w) && mbar_wait(&bar_k[0], 0, w);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) {
+            issue_s(t, 0);
+            mma_commit(&bar_s[t]);
+          }
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int s = j % C::kStages;
+        if (!mbar_wait(&bar_v[s], (j / C::kStages) & 1, w)) break;
+        bool k_next = false;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!mbar_wait(&bar_p[t], j & 1, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          if (j + 1 < nkv[t]) {
+            const int s1 = (j + 1) % C::kStages;
+            if (!k_next) {
+              if (!mbar_wait(&bar_k[s1], ((j + 1) / C::kStages) & 1, w)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, s1);
+          }
+          mma_commit(&bar_s[t]);
+        }
+        if (ok) mma_commit(&bar_free[s]);
+      }
+      // every MMA issued must be complete before tensor memory is released
+      mma_commit(&bar_done);
+      mbar_wait_drain(&bar_done, 0, p.limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int t = warp >> 2;
+    const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
+    const int r = quad * 32 + lane;     // row within the query tile
+    const int qt = qt0 + t;
+    const int n = nkv[t];
+    if (n > 0) {
+      const int i = qt * kBM + r;       // row within the sequence
+      const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+      const uint32_t t_s = tmem + lane_off + t * 128;
+      const uint32_t t_o = tmem + lane_off + 256 + t * 128;
+      float m_ref = -INFINITY;          // reference maximum of the exponentials (log2 units)
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (!mbar_wait(&bar_s[t], j & 1, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+        const int k0 = j * kBN;
+        const bool mask = (p.causal && j == qt) || (k0 + kBN > len);
+        const int kmax = min(len, p.causal ? i + 1 : len) - k0;  // keys [k0, k0 + kmax) allowed
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(sr[c][e]) * p.c2;
+            if (mask && c * 32 + e >= kmax) x = -INFINITY;
+            sr[c][e] = __float_as_uint(x);
+            mt = fmaxf(mt, x);
+          }
+        const float m_new = fmaxf(m_ref, mt);
+        float alpha = 1.f;
+        const bool grow = m_new > m_ref + kRescaleThreshold;
+        if (grow) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+          l *= alpha;
+        }
+        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int e0 = 64 * hf + 2 * c;
+            const float p0 = ex2_approx(__uint_as_float(sr[e0 >> 5][e0 & 31]) - mu);
+            const float p1 = ex2_approx(__uint_as_float(sr[(e0 + 1) >> 5][(e0 + 1) & 31]) - mu);
+            rs += p0 + p1;
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(t_s + 32 * hf, pk);
+        }
+        l += rs;
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // accumulator rows rescaled in place: the previous PV is complete (the
+          // wait on bar_s covers it) and this tile's PV waits for bar_p below
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p[t]);
+      }
+      if (ok && mbar_wait(&bar_s[t], n & 1, w)) {
+        tc_fence_after();
+        const bool row_ok = i < len;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = p.o + (out_base + i) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_ld_wait(o);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+              u.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+              u.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+              u.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+              dst[v4] = u;
+            }
+          }
+        }
+        if (row_ok) p.lse[out_base + i] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
+  using C = FwdCfg<D>;
+  FwdParams fp;
+  if (!make_bf16_map(&fp.tq, p.q, p, kBM) || !make_bf16_map(&fp.tk, p.k, p, kBN) ||
+      !make_bf16_map(&fp.tv, p.v, p, kBN))
+    return cudaErrorInvalidValue;
+  fp.o = static_cast<__nv_bfloat16*>(p.o);
+  fp.lse = p.lse;
+  fp.cu = p.cu;
+  fp.status = p.status;
+  fp.limit_ns = p.wait_limit_ns;
+  fp.B = p.B;
+  fp.H = p.H;
+  fp.N = p.N;
+  fp.T = p.T;
+  fp.c2 = p.scale * kLog2e;
+  fp.causal = p.causal;
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_qt = (p.N + kBM - 1) / kBM;
+  dim3 grid((n_qt + 1) / 2, p.H, p.B);
+  tc_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s) {
+  if (p.D == 64) return launch_fwd_d<64>(p, s);
+  if (p.D == 128) return launch_fwd_d<128>(p, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,168 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library, libfa_gb300.so.
+ *
+ * What is computed (tensortonic.com "FlashAttention", sections 1, 4-7;
+ * wiki.ai-engineering.at "Flash Attention", The Core Problem):
+ *
+ *     S = scale * Q K^T  (+ causal mask: key j allowed for query i iff j <= i)
+ *     O = softmax_rows(S) V
+ *     L_i = m_i + log(l_i)  = log sum_j exp(S_ij)        (natural log)
+ *
+ * computed tile by tile with a running (m, l, u) state per query row; the
+ * n x n score matrix is never written to device memory.  The backward pass
+ * rebuilds every weight as P_ij = exp(S_ij - L_i) (section 7) and forms
+ *
+ *     D_i = rowsum(dO o O),  dS = P o (dO V^T - D),
+ *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+ *
+ * Layouts (all row-major, contiguous, element strides implied):
+ *   dense  (cu_seqlens == NULL): Q, K, V, O, dO, dQ, dK, dV are [B, H, N, D];
+ *          lse is [B, H, N] float32.
+ *   packed (cu_seqlens != NULL): B sequences packed along one token axis of
+ *          length total_tokens = cu_seqlens[B]; tensors are [H, total_tokens, D]
+ *          and lse is [H, total_tokens].  Sequence s owns tokens
+ *          cu_seqlens[s] .. cu_seqlens[s+1]-1 of every head and attends only
+ *          within itself.  N is the maximum sequence length (grid sizing only).
+ *   Causal alignment is square / top-left within each sequence.
+ *
+ * Types: FA_BF16 -- Q, K, V, O, dO, dQ, dK, dV are bfloat16; arithmetic is
+ *          tcgen05 tensor-core bf16 x bf16 -> fp32 for the five contractions,
+ *          fp32 for softmax; head width D must be 64 or 128.
+ *        FA_F32  -- all of them float32; arithmetic is fp32 FMA (no TF32);
+ *          D must be 32, 64 or 128.
+ *        lse is always float32.
+ *
+ * Ownership and memory: every pointer argument is a DEVICE pointer owned by the
+ * caller (except where stated); the library allocates no device memory and
+ * keeps no state beyond cached per-device properties and a per-device status
+ * word.  All pointers to tensors must be 16-byte aligned.
+ *
+ * Asynchrony: fa_fwd and fa_bwd validate their arguments on the host, enqueue
+ * kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ * return without waiting.  A return of FA_OK means "enqueued".  Faults the
+ * kernels detect themselves (malformed cu_seqlens, a bounded wait that ran
+ * out) are latched in a per-device status word read by
+ * fa_get_last_device_error.
+ *
+ * Errors: invalid arguments return an error code before anything is launched;
+ * nothing aborts the process.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = -1,      /* NULL pointer, negative size, non-finite scale, bad cu_seqlens */
+  FA_ERR_UNSUPPORTED = -2,  /* head width or dtype this build has no kernel for */
+  FA_ERR_ALIGN = -3,        /* a tensor pointer is not 16-byte aligned */
+  FA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed (launch, tensor map) */
+  FA_ERR_TIMEOUT = -5,      /* a kernel's bounded wait expired (reported by fa_get_last_device_error) */
+  FA_ERR_WORKSPACE = -6     /* workspace NULL, misaligned or smaller than fa_bwd_workspace_size */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/*
+ * Forward pass.  tensortonic.com "FlashAttention" sections 5-7.
+ *   q, k, v       in : [B,H,N,D] (dense) or [H,T,D] (packed), dtype
+ *   o             out: same layout and dtype as q; O = u / l rounded to nearest
+ *   lse           out: float32 [B,H,N] or [H,T]; natural-log L = m + log(l)
+ *   B, H, N, D    batch (or number of packed sequences), heads, tokens (or max
+ *                 sequence length when packed), head width; B, H, N >= 0
+ *   scale         multiplies Q K^T before the mask and softmax (1/sqrt(D) is
+ *                 the usual value); must be finite
+ *   causal        0 = full attention, 1 = key j allowed for query i iff j <= i
+ *   cu_seqlens    NULL for dense; else DEVICE int32[B+1], non-decreasing,
+ *                 cu_seqlens[0] = 0, cu_seqlens[B] = total_tokens, every
+ *                 length <= N.  A violation found on the device skips that
+ *                 sequence and latches FA_ERR_INVALID.
+ *   total_tokens  T for packed input (ignored when cu_seqlens == NULL)
+ *   stream        cudaStream_t
+ * Rows of a packed sequence of length 0 produce nothing.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int D, float scale, int causal,
+                 const int32_t* cu_seqlens, int total_tokens,
+                 fa_dtype dtype, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D_i (float32 per row) and, for the
+ * tensor-core path, a float32 dQ accumulator of the shape of Q.  Pure host
+ * arithmetic; never fails (returns 0 for invalid sizes).
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int D, const int32_t* cu_seqlens,
+                             int total_tokens, fa_dtype dtype);
+
+/*
+ * Backward pass.  tensortonic.com "FlashAttention" section 7 (weights rebuilt
+ * as exp(s_ij - L_i)); gradient algebra in the file header.
+ *   q, k, v, o    in : as passed to / produced by fa_fwd
+ *   lse           in : float32 L from fa_fwd
+ *   dout          in : upstream gradient dO, same layout and dtype as o
+ *   dq, dk, dv    out: gradients, same layout and dtype as q (overwritten)
+ *   workspace     DEVICE scratch of at least fa_bwd_workspace_size(...)
+ *                 bytes, 256-byte aligned, owned by the caller; its contents
+ *                 on entry do not matter; calls sharing a workspace must not
+ *                 overlap on the device
+ *   other arguments as for fa_fwd
+ * dK and dV are written deterministically; dQ is accumulated in float32 with
+ * atomic adds on the tensor-core path, so its last bits may vary run to run.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv,
+                 int B, int H, int N, int D, float scale, int causal,
+                 const int32_t* cu_seqlens, int total_tokens, fa_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static English text for a status code. */
+const char* fa_strerror(fa_status status);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's latched
+ * kernel status: FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran
+ * out; the kernel stopped its work, released its tensor memory and returned)
+ * or FA_ERR_INVALID (malformed cu_seqlens seen on the device).  Returns
+ * FA_ERR_CUDA if the synchronisation itself fails.
+ */
+fa_status fa_get_last_device_error(void* stream);
+
+/*
+ * Upper bound, in nanoseconds, on every bounded wait inside the kernels
+ * (default 2e9 ns).  Applies to launches made after the call, on every device.
+ * Values below 1000 are raised to 1000.
+ */
+void fa_set_wait_limit_ns(unsigned long long limit_ns);
+
+/*
+ * Failure-detection self-test: launches one CTA that waits, with the current
+ * wait limit, on a shared-memory barrier nothing ever signals, then returns
+ * fa_get_last_device_error(stream) -- FA_ERR_TIMEOUT when the bounded wait
+ * works.  No fault, trap or hang is involved.
+ */
+fa_status fa_selftest_wait_timeout(void* stream);
+
+/*
+ * Name of the kernel family fa_fwd / fa_bwd launch for this dtype and head
+ * width ("tcgen05" or "simt_f32"), or NULL when unsupported.  Host only.
+ */
+const char* fa_path_name(fa_dtype dtype, int D);
+
+/*
+ * Number of kernels this library has launched in this process (all devices,
+ * all entry points, including failed launches it detected).  Host only.
+ */
+unsigned long long fa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

