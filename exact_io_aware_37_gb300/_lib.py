@@ -27,6 +27,7 @@ SIGNATURES = {
     "fa_selftest_wait_timeout": (_int, [_vp]),
     "fa_path_name": (_c.c_char_p, [_int, _int]),
     "fa_launch_count": (_c.c_ulonglong, []),
+    "fa_last_error_detail": (_c.c_char_p, []),
 }
 
 
@@ -57,4 +58,5 @@ class FAError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
         msg = lib().fa_strerror(status).decode()
-        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg})")
+        detail = lib().fa_last_error_detail().decode() if status == -4 else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({msg})" + (f" [{detail}]" if detail else ""))

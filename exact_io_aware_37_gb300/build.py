@@ -8,6 +8,7 @@ machine without a GPU and exports only the C ABI of include/fa.h.
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -21,6 +22,14 @@ LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu"]
+
+# The tensor-core kernels launch 384 threads and then move registers between
+# warpgroups with setmaxnreg (224 + 224 + 56 per thread).  That split is only
+# safe when every thread starts with 168 registers; a kernel that ptxas
+# compiled with fewer would wait forever in setmaxnreg.inc, so the build
+# refuses it.
+SPLIT_KERNELS = ("tc_fwd_kernel", "tc_bwd_kernel")
+SPLIT_LAUNCH_REGS = 168
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
@@ -48,6 +57,27 @@ def up_to_date():
     return all(os.path.getmtime(f) <= t for f in _inputs() + [os.path.abspath(__file__)])
 
 
+def check_register_split(log_text, src):
+    """Raise unless every split kernel in a ptxas -v log uses SPLIT_LAUNCH_REGS;
+    returns how many such kernels the log reports."""
+    current = None
+    seen = 0
+    for line in log_text.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current and any(k in current for k in SPLIT_KERNELS):
+            regs = int(m.group(1))
+            if regs != SPLIT_LAUNCH_REGS:
+                raise RuntimeError(f"{src}: {current} compiled with {regs} registers; the warpgroup register "
+                                   f"split needs exactly {SPLIT_LAUNCH_REGS}")
+            seen += 1
+            current = None
+    return seen
+
+
 def build(force=False, verbose=False, jobs=None):
     """Compile and link; returns the library path.  Raises on failure."""
     if not force and up_to_date():
@@ -64,6 +94,8 @@ def build(force=False, verbose=False, jobs=None):
             f.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr[-6000:]}")
+        if check_register_split(r.stdout + r.stderr, src) == 0 and src.startswith("fa_tc_"):
+            raise RuntimeError(f"{src}: no register report found for the split kernels")
         if verbose:
             sys.stderr.write(r.stderr)
         return obj

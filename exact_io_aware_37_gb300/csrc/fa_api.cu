@@ -2,6 +2,8 @@
 // per-device status word, workspace carving and kernel dispatch.
 #include <math.h>
 
+#include <stdio.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -42,12 +44,13 @@ cudaError_t status_word(unsigned** out) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The tensor-core kernels cover bf16 with D in {64, 128}.
-constexpr bool kHaveTcFwd = false;
-constexpr bool kHaveTcBwd = false;
+constexpr bool kHaveTcFwd = true;
+constexpr bool kHaveTcBwd = true;
 bool use_tensor_cores(fa_dtype dt, int D) { return dt == FA_BF16 && (D == 64 || D == 128); }
 
 fa_status validate(int B, int H, int N, int D, float scale, int causal, const int32_t* cu, int T, fa_dtype dt) {
   if (B < 0 || H < 0 || N < 0 || D <= 0) return FA_ERR_INVALID;
+  if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;  // grid y / z limits
   if (!isfinite(scale)) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (dt != FA_BF16 && dt != FA_F32) return FA_ERR_UNSUPPORTED;
@@ -75,6 +78,13 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 void note_launches(unsigned n) { g_launches.fetch_add(n); }
+
+thread_local char g_detail[256];
+
+cudaError_t note_error(const char* step, cudaError_t e) {
+  if (e != cudaSuccess) snprintf(g_detail, sizeof(g_detail), "%s: %s", step, cudaGetErrorString(e));
+  return e;
+}
 
 // Failure-detection self-test kernel: waits on a barrier nobody signals.
 __global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
@@ -117,12 +127,15 @@ const char* fa_strerror(fa_status s) {
 }
 
 const char* fa_path_name(fa_dtype dt, int D) {
-  if (dt == FA_BF16 && (D == 64 || D == 128)) return kHaveTcFwd ? "tcgen05" : "simt_bf16";
+  if (dt == FA_BF16 && (D == 64 || D == 128))
+    return kHaveTcFwd ? (kHaveTcBwd ? "tcgen05" : "tcgen05_fwd+simt_bwd") : "simt_bf16";
   if (dt == FA_F32 && (D == 32 || D == 64 || D == 128)) return "simt_f32";
   return nullptr;
 }
 
 unsigned long long fa_launch_count(void) { return g_launches.load(); }
+
+const char* fa_last_error_detail(void) { return g_detail; }
 
 void fa_set_wait_limit_ns(unsigned long long limit_ns) {
   g_wait_limit_ns.store(limit_ns < 1000ull ? 1000ull : limit_ns);
@@ -173,7 +186,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
   p.scale = scale; p.causal = causal; p.cu = cu;
   p.wait_limit_ns = g_wait_limit_ns.load();
-  if (status_word(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+  g_detail[0] = 0;
+  if (note_error("status word", status_word(&p.status)) != cudaSuccess) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = (kHaveTcFwd && use_tensor_cores(dt, D)) ? launch_tc_fwd(p, s) : launch_simt_fwd(p, dt, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -204,7 +218,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.dq_acc = use_tensor_cores(dt, D)
                  ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)rows * 4, 256))
                  : nullptr;
-  if (status_word(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+  g_detail[0] = 0;
+  if (note_error("status word", status_word(&p.status)) != cudaSuccess) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_preprocess(p, dt, p.dq_acc != nullptr, s);
   if (e == cudaSuccess) e = (kHaveTcBwd && use_tensor_cores(dt, D)) ? launch_tc_bwd(p, s) : launch_simt_bwd(p, dt, s);

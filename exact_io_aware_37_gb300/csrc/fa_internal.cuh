@@ -70,6 +70,10 @@ __device__ __forceinline__ void st_elem(__nv_bfloat16* p, long long i, float x) 
 // Counts kernel launches (read by fa_launch_count); every launcher bumps it.
 void note_launches(unsigned n);
 
+// Records why a host-side CUDA step failed (read by fa_last_error_detail) and
+// passes the error through.
+cudaError_t note_error(const char* step, cudaError_t e);
+
 // ---- launchers (defined in the kernel translation units) -------------------
 cudaError_t launch_simt_fwd(const Problem& p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_simt_bwd(const Problem& p, fa_dtype dt, cudaStream_t s);

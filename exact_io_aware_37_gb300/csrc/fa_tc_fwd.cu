@@ -8,7 +8,7 @@
 // MMAs whose accumulators live in tensor memory (TMEM), and only O = u / l and
 // L = m + log(l) are written to device memory (section 7).
 //
-// Warp roles (10 warps):
+// Warp roles (12 warps; warps 10-11 only complete the third warpgroup):
 //   warps 0-3  softmax for query tile 0, warps 4-7 for query tile 1: one
 //              thread per query row (its TMEM lane), so row max and row sum
 //              are thread-local; exp2 of scores pre-scaled by scale*log2(e);
@@ -17,6 +17,9 @@
 //              running maximum grows by more than 2^8 (a lazy rescale: the
 //              final u / l uses the same reference maximum, so it is exact),
 //              and run the epilogue.
+//   The softmax warpgroups raise their register limit to 224 and the third
+//   warpgroup lowers its to 56 (setmaxnreg) so the 128 scores of a row stay
+//   in registers.
 //   warp 8     TMA producer: Q tiles once, then K_j / V_j into a ring of
 //              shared-memory stages (mbarrier full/empty pairs).
 //   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T, then, once the
@@ -43,7 +46,7 @@ using namespace ptx;
 
 constexpr int kBM = 128;              // query rows per tile
 constexpr int kBN = 128;              // keys per tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 2 softmax warpgroups + 1 support warpgroup
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
@@ -77,7 +80,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 template <int D>
-__global__ void __maxnreg__(200) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -146,110 +149,9 @@ __global__ void __maxnreg__(200) tc_fwd_kernel(const __grid_constant__ FwdParams
   const uint32_t tmem = tmem_base_sh;
   const WaitCtx w{&abort_flag, p.status, p.limit_ns};
 
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tq);
-      tma_prefetch_desc(&p.tk);
-      tma_prefetch_desc(&p.tv);
-      const int nq = nkv[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bar_q, nq * C::kTileBytes);
-      for (int t = 0; t < nq; ++t)
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
-                      row0 + (qt0 + t) * kBM, slab);
-      int issued = 0;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % C::kStages, round = j / C::kStages;
-        if (round > 0 && !mbar_wait(&bar_free[s], (round - 1) & 1, w)) break;
-        mbar_arrive_expect_tx(&bar_k[s], C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_k[s], hf * 64,
-                      row0 + j * kBN, slab);
-        mbar_arrive_expect_tx(&bar_v[s], C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_v[s], hf * 64,
-                      row0 + j * kBN, slab);
-        issued = j + 1;
-      }
-      if (abort_flag) {
-        // let copies already in flight land before the CTA's memory is released
-        mbar_wait_drain(&bar_q, 0, p.limit_ns);
-        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
-          mbar_wait_drain(&bar_k[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
-          mbar_wait_drain(&bar_v[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
-        }
-      }
-    }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(kBM, kBN, false, false);
-      const uint32_t id_o = idesc_bf16(kBM, D, false, true);
-      const uint32_t sq = smem_u32(smem + C::kQOff);
-      const uint32_t sk = smem_u32(smem + C::kKOff);
-      const uint32_t sv = smem_u32(smem + C::kVOff);
-      // S_t = Q_t K^T (both K-major): D/16 MMAs of K = 16
-      auto issue_s = [&](int t, int s) {
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * C::kHalfBytes + (ks & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sq + t * C::kTileBytes + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sk + s * C::kTileBytes + off, 16, 1024);
-          mma_ss(tmem + t * 128, ad, bd, id_s, ks > 0 ? 1u : 0u);
-        }
-      };
-      // O_t += P_t V (P from TMEM, V MN-major): 8 MMAs of K = 16 keys
-      auto issue_pv = [&](int t, int s, bool acc) {
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t bd = sdesc_sw128(sv + s * C::kTileBytes + ks * 2048, C::kHalfBytes, 1024);
-          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, id_o, (acc || ks > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(&bar_q, 0, w) && mbar_wait(&bar_k[0], 0, w);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0) {
-            issue_s(t, 0);
-            mma_commit(&bar_s[t]);
-          }
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int s = j % C::kStages;
-        if (!mbar_wait(&bar_v[s], (j / C::kStages) & 1, w)) break;
-        bool k_next = false;
-        for (int t = 0; t < 2; ++t) {
-          if (j >= nkv[t]) continue;
-          if (!mbar_wait(&bar_p[t], j & 1, w)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          if (j + 1 < nkv[t]) {
-            const int s1 = (j + 1) % C::kStages;
-            if (!k_next) {
-              if (!mbar_wait(&bar_k[s1], ((j + 1) / C::kStages) & 1, w)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_next = true;
-            }
-            issue_s(t, s1);
-          }
-          mma_commit(&bar_s[t]);
-        }
-        if (ok) mma_commit(&bar_free[s]);
-      }
-      // every MMA issued must be complete before tensor memory is released
-      mma_commit(&bar_done);
-      mbar_wait_drain(&bar_done, 0, p.limit_ns);
-    }
-  } else {
+  if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
+    setmaxnreg_inc<kComputeRegs>();
     const int t = warp >> 2;
     const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
     const int r = quad * 32 + lane;     // row within the query tile
@@ -264,7 +166,7 @@ __global__ void __maxnreg__(200) tc_fwd_kernel(const __grid_constant__ FwdParams
       float l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        if (!mbar_wait(&bar_s[t], j & 1, w)) {
+        if (!warp_wait(&bar_s[t], j & 1, w)) {
           ok = false;
           break;
         }
@@ -329,7 +231,7 @@ __global__ void __maxnreg__(200) tc_fwd_kernel(const __grid_constant__ FwdParams
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p[t]);
       }
-      if (ok && mbar_wait(&bar_s[t], n & 1, w)) {
+      if (ok && warp_wait(&bar_s[t], n & 1, w)) {
         tc_fence_after();
         const bool row_ok = i < len;
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -355,6 +257,110 @@ __global__ void __maxnreg__(200) tc_fwd_kernel(const __grid_constant__ FwdParams
         if (row_ok) p.lse[out_base + i] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       }
     }
+  } else {
+    // warps 8-11: producer, MMA issuer and two idle warps completing the warpgroup
+    setmaxnreg_dec<kSupportRegs>();
+    if (warp == kTmaWarp && lane == 0) {
+      // ---------------------------------------------------------- producer
+      tma_prefetch_desc(&p.tq);
+      tma_prefetch_desc(&p.tk);
+      tma_prefetch_desc(&p.tv);
+      const int nq = nkv[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bar_q, nq * C::kTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
+                      row0 + (qt0 + t) * kBM, slab);
+      int issued = 0;
+      for (int j = 0; j < nmax; ++j) {
+        const int s = j % C::kStages, round = j / C::kStages;
+        if (round > 0 && !mbar_wait(&bar_free[s], (round - 1) & 1, w)) break;
+        mbar_arrive_expect_tx(&bar_k[s], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_k[s], hf * 64,
+                      row0 + j * kBN, slab);
+        mbar_arrive_expect_tx(&bar_v[s], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_v[s], hf * 64,
+                      row0 + j * kBN, slab);
+        issued = j + 1;
+      }
+      if (abort_flag) {
+        // let copies already in flight land before the CTA's memory is released
+        mbar_wait_drain(&bar_q, 0, p.limit_ns);
+        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+          mbar_wait_drain(&bar_k[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
+          mbar_wait_drain(&bar_v[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
+        }
+      }
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t id_s = idesc_bf16(kBM, kBN, false, false);
+      const uint32_t id_o = idesc_bf16(kBM, D, false, true);
+      // Descriptors are built once and advanced by adding (byte offset >> 4)
+      // to their start-address field.
+      const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kVOff), C::kHalfBytes, 1024);
+      // S_t = Q_t K^T (both K-major): D/16 MMAs of K = 16
+      auto issue_s = [&](int t, int s) {
+        const uint64_t a = dq0 + ((t * C::kTileBytes) >> 4);
+        const uint64_t bk = dk0 + ((s * C::kTileBytes) >> 4);
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + t * 128, a + off, bk + off, id_s, ks > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V (P from TMEM, V MN-major): 8 MMAs of K = 16 keys
+      auto issue_pv = [&](int t, int s, bool acc) {
+        const uint64_t bv = dv0 + ((s * C::kTileBytes) >> 4);
+#pragma unroll 1
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bv + ((ks * 2048) >> 4), id_o,
+                 (acc || ks > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(&bar_q, 0, w) && mbar_wait(&bar_k[0], 0, w);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) {
+            issue_s(t, 0);
+            mma_commit(&bar_s[t]);
+          }
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int s = j % C::kStages;
+        if (!mbar_wait(&bar_v[s], (j / C::kStages) & 1, w)) break;
+        bool k_next = false;
+        for (int t = 0; t < 2; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!mbar_wait(&bar_p[t], j & 1, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          if (j + 1 < nkv[t]) {
+            const int s1 = (j + 1) % C::kStages;
+            if (!k_next) {
+              if (!mbar_wait(&bar_k[s1], ((j + 1) / C::kStages) & 1, w)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              k_next = true;
+            }
+            issue_s(t, s1);
+          }
+          mma_commit(&bar_s[t]);
+        }
+        if (ok) mma_commit(&bar_free[s]);
+      }
+      // every MMA issued must be complete before tensor memory is released
+      mma_commit(&bar_done);
+      mbar_wait_drain(&bar_done, 0, p.limit_ns);
+    }
   }
 
   tc_fence_before();
@@ -368,7 +374,7 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   FwdParams fp;
   if (!make_bf16_map(&fp.tq, p.q, p, kBM) || !make_bf16_map(&fp.tk, p.k, p, kBN) ||
       !make_bf16_map(&fp.tv, p.v, p, kBN))
-    return cudaErrorInvalidValue;
+    return note_error("forward tensor map encode", cudaErrorInvalidValue);
   fp.o = static_cast<__nv_bfloat16*>(p.o);
   fp.lse = p.lse;
   fp.cu = p.cu;
@@ -381,12 +387,12 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   fp.c2 = p.scale * kLog2e;
   fp.causal = p.causal;
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) return note_error("forward smem attribute", e);
   const int n_qt = (p.N + kBM - 1) / kBM;
   dim3 grid((n_qt + 1) / 2, p.H, p.B);
   tc_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
   note_launches(1);
-  return cudaGetLastError();
+  return note_error("forward launch", cudaGetLastError());
 }
 
 }  // namespace

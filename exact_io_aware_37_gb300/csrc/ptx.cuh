@@ -82,6 +82,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Warp-uniform form for warps whose lanes all wait (the softmax / gradient
+// warps): every lane gets the same answer, so a warp never splits in front of
+// a .sync.aligned tensor-memory instruction when a wait gives up.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w)) != 0;
+}
+
 // Wait that ignores the abort flag (used only while winding down, to let
 // copies already in flight land before the CTA exits).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
@@ -90,6 +97,28 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+
+// ------------------------------------------------------------------ register split
+// Warpgroup-wide (all 128 threads) change of the per-thread register limit.
+// The tensor-core kernels launch 384 threads at kLaunchRegs registers each;
+// the two compute warpgroups raise theirs to kComputeRegs and the producer /
+// MMA warpgroup lowers its to kSupportRegs.  The split must not exceed the
+// launch budget or the raise would wait forever: the static_assert checks the
+// arithmetic and build.py checks that ptxas gave the kernels kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kComputeRegs = 224;
+constexpr int kSupportRegs = 56;
+static_assert(2 * 128 * kComputeRegs + 128 * kSupportRegs <= 384 * kLaunchRegs,
+              "register split exceeds the launch budget");
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ TMA

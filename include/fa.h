@@ -151,9 +151,18 @@ fa_status fa_selftest_wait_timeout(void* stream);
 
 /*
  * Name of the kernel family fa_fwd / fa_bwd launch for this dtype and head
- * width ("tcgen05" or "simt_f32"), or NULL when unsupported.  Host only.
+ * width ("tcgen05" for bf16, "simt_f32" for float32), or NULL when
+ * unsupported.  Host only.
  */
 const char* fa_path_name(fa_dtype dtype, int D);
+
+/*
+ * Human-readable detail of the most recent FA_ERR_CUDA returned on the
+ * calling host thread (which step failed and the CUDA error text); an empty
+ * string when there is none.  The pointer stays valid until the next call on
+ * this thread.
+ */
+const char* fa_last_error_detail(void);
 
 /*
  * Number of kernels this library has launched in this process (all devices,
