@@ -18,7 +18,7 @@ import torch
 from ._lib import FA_BF16, FA_F32, FAError, lib, library_path  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
-           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "forward", "backward",
+           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "forward", "backward",
            "FAError"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
@@ -119,6 +119,30 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_seqlens=Non
                       _ptr(workspace), workspace.numel(), _stream(stream))
     if st != 0:
         raise FAError(st, "fa_bwd")
+
+
+def fa_bwd_static_ws(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_seqlens=None, max_seqlen=None,
+                     stream=None):
+    """fa_bwd without a workspace argument: the library's own fixed device
+    buffer (FA_BWD_STATIC_WS_BYTES, 16 MiB) serves as scratch, for callers
+    that cannot allocate device memory.  Calls sharing a device must not
+    overlap on the GPU; problems needing more scratch raise FAError
+    (FA_ERR_WORKSPACE)."""
+    _check(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens)
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    st = lib().fa_bwd_static_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                _ptr(dv), B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T, _DT[q.dtype],
+                                _stream(stream))
+    if st != 0:
+        err = FAError(st, "fa_bwd_static_ws")
+        detail = lib().fa_last_error_detail().decode()
+        if detail and detail not in str(err):
+            err = FAError(st, f"fa_bwd_static_ws [{detail}]")
+        raise err
+
+
+STATIC_WS_BYTES = 16 << 20
 
 
 def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):

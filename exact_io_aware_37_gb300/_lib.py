@@ -21,6 +21,8 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (_sz, [_int, _int, _int, _int, _vp, _int, _int]),
     "fa_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int,
                       _vp, _int, _int, _vp, _sz, _vp]),
+    "fa_bwd_static_ws": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int,
+                                _vp, _int, _int, _vp]),
     "fa_strerror": (_c.c_char_p, [_int]),
     "fa_get_last_device_error": (_int, [_vp]),
     "fa_set_wait_limit_ns": (None, [_c.c_ulonglong]),

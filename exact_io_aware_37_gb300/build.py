@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
-SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu"]
+SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_static_ws.cu"]
 
 # The tensor-core kernels launch 384 threads and then move registers between
 # warpgroups with setmaxnreg (224 + 224 + 56 per thread).  That split is only

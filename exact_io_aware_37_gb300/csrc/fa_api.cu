@@ -86,6 +86,8 @@ cudaError_t note_error(const char* step, cudaError_t e) {
   return e;
 }
 
+void note_detail(const char* msg) { snprintf(g_detail, sizeof(g_detail), "%s", msg); }
+
 // Failure-detection self-test kernel: waits on a barrier nobody signals.
 __global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;

@@ -73,6 +73,8 @@ void note_launches(unsigned n);
 // Records why a host-side CUDA step failed (read by fa_last_error_detail) and
 // passes the error through.
 cudaError_t note_error(const char* step, cudaError_t e);
+// Records a plain message as the detail of the failure being returned.
+void note_detail(const char* msg);
 
 // ---- launchers (defined in the kernel translation units) -------------------
 cudaError_t launch_simt_fwd(const Problem& p, fa_dtype dt, cudaStream_t s);

@@ -122,6 +122,41 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const int32_t* cu_seqlens, int total_tokens, fa_dtype dtype,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment convenience, not a step of the
+ * method.
+ *
+ * fa_bwd needs scratch (D_i per row and, for bf16, a float32 dQ accumulator)
+ * that the caller allocates.  Some callers cannot: a plugin inside a host
+ * application that owns all device memory through its own pool and forbids
+ * direct cudaMalloc, or a latency-critical loop that must not pay for a
+ * cudaMalloc (which may synchronise the device).  fa_bwd_static_ws takes the
+ * same arguments as fa_bwd minus the workspace and uses instead a fixed
+ * array of FA_BWD_STATIC_WS_BYTES that the library keeps in device memory on
+ * every GPU that loads it, until the process exits.  It calls no allocator.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Problems whose fa_bwd_workspace_size exceeds FA_BWD_STATIC_WS_BYTES are
+ *     rejected with FA_ERR_WORKSPACE before anything is launched
+ *     (fa_last_error_detail says why).  16 MiB covers, e.g., 32K rows at
+ *     D = 128 or 64K rows at D = 64 in bf16, and 4M rows in float32.
+ *   - Every call on a device shares the one array.  Its previous contents do
+ *     not matter (the backward rewrites D_i and zeroes the dQ accumulator
+ *     before reading them), but calls that overlap on the GPU -- on different
+ *     streams or from different host threads -- race on it and give wrong
+ *     gradients.  Serialise them.
+ * Results are those of fa_bwd with a caller workspace.
+ */
+#define FA_BWD_STATIC_WS_BYTES ((size_t)16 << 20)
+fa_status fa_bwd_static_ws(const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout,
+                           void* dq, void* dk, void* dv,
+                           int B, int H, int N, int D, float scale, int causal,
+                           const int32_t* cu_seqlens, int total_tokens, fa_dtype dtype,
+                           void* stream);
+
 /* Static English text for a status code. */
 const char* fa_strerror(fa_status status);
 
