@@ -153,6 +153,7 @@ fa_status fa_get_last_device_error(void* stream) {
   if (v != 0 && cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
   if (v & kDevTimeout) return FA_ERR_TIMEOUT;
   if (v & kDevBadSeqlens) return FA_ERR_INVALID;
+  if (v & kDevInternal) return FA_ERR_CUDA;
   return FA_OK;
 }
 

@@ -13,6 +13,7 @@ namespace fa {
 enum : unsigned {
   kDevTimeout = 1u,     // a bounded wait ran out
   kDevBadSeqlens = 2u,  // cu_seqlens violated its contract
+  kDevInternal = 4u,    // a kernel found its launch environment unusable (e.g. misaligned shared memory)
 };
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -15,9 +15,13 @@
 //     dP^T = V dO^T     -> TMEM [128,256)
 //     dV  += P^T dO     (P^T read from TMEM)  -> TMEM [256,256+D)
 //     dK  += dS^T Q     (dS^T from shared)    -> TMEM [384,384+D)
-//     dQ_i = dS K       (dS = the same shared buffer read MN-major) -> TMEM [0,D)
+//     dQ_i^T = K^T dS^T (dS^T and K read MN-major) -> TMEM [0,128)   (D = 128)
+//     dQ_i   = dS K                                 -> TMEM [0,D)     (D = 64)
 // The dQ tile is added into a float32 accumulator in device memory with
-// vector atomics; a small kernel then scales and rounds it to bf16.
+// atomics (at D = 128 one warp's reductions cover one contiguous 128-byte
+// line); a small kernel then scales and rounds it to bf16.  Q and dO tiles
+// (with their L and D values) stream through a two-stage ring so the next
+// step's loads overlap the current step.
 //
 // Warp roles (12 warps): warps 0-3 and 4-7 each own half of the 128 query
 // columns of S^T / dP^T for all 128 key rows (one key row per thread, its
@@ -60,43 +64,61 @@ struct BwdParams {
   int causal;
 };
 
-template <int D>
-struct BwdCfg {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kHalfBytes = 16384;  // 128 rows x 128 bytes
-  static constexpr int kHalves = D / 64;
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kTileBytes;
-  static constexpr int kQOff = 2 * kTileBytes;
-  static constexpr int kDOOff = 3 * kTileBytes;
-  static constexpr int kDSOff = 4 * kTileBytes;          // dS^T, [128 keys][128 queries] bf16
-  static constexpr int kLOff = kDSOff + 2 * kHalfBytes;  // 128 floats: L_i * log2(e)
-  static constexpr int kDvOff = kLOff + 512;             // 128 floats: D_i
-  static constexpr int kSmemBytes = kDvOff + 512 + 1024;
-};
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
 
 template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kHalfBytes = 16384;  // 128 rows x 128 bytes
+  static constexpr int kHalves = D / 64;
+  // dQ^T = K^T dS^T (head width on TMEM lanes: coalesced reductions) needs
+  // M = D = 128; at D = 64 the kernel forms dQ = dS K (queries on lanes).
+  static constexpr bool kDqTransposed = D == 128;
+  // Dynamic shared memory only (the tiles need a 1024-byte aligned base, which
+  // the kernel checks): K, V, a 2-stage ring of Q and dO, dS^T, then the L / D
+  // vectors of both stages and the barriers.
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;         // + stage * kTileBytes
+  static constexpr int kDOOff = 4 * kTileBytes;        // + stage * kTileBytes
+  static constexpr int kDSOff = 6 * kTileBytes;        // [128 keys][128 queries] bf16
+  static constexpr int kLOff = kDSOff + 2 * kHalfBytes;  // 2 x 128 floats: L_i * log2(e)
+  static constexpr int kDvOff = kLOff + 1024;            // 2 x 128 floats: D_i
+  static constexpr int kBarOff = kDvOff + 1024;          // 16 mbarriers
+  static constexpr int kMiscOff = kBarOff + 16 * 8;      // TMEM base, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static_assert(kSmemBytes <= 232448, "backward tiles exceed the shared-memory limit");
+};
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  __shared__ __align__(8) uint64_t bar_kv, bar_qf, bar_qe, bar_of, bar_oe;
-  __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dq, bar_dqfree, bar_done;
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_flag;
-
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, h = blockIdx.y, kt = blockIdx.x;
+  if (smem_u32(smem) & 1023u) {  // the swizzled tile layout needs a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicOr(p.status, kDevInternal);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_qf = bars + 1;  // [2] Q tile + L / D of a stage loaded
+  uint64_t* bar_qe = bars + 3;  // [2] stage's Q / L / D free (dK done)
+  uint64_t* bar_of = bars + 5;  // [2] dO tile loaded
+  uint64_t* bar_oe = bars + 7;  // [2] dO stage free (dV done)
+  uint64_t* bar_s = bars + 9;
+  uint64_t* bar_dp = bars + 10;
+  uint64_t* bar_p = bars + 11;
+  uint64_t* bar_ds = bars + 12;
+  uint64_t* bar_dq = bars + 13;
+  uint64_t* bar_dqfree = bars + 14;
+  uint64_t* bar_done = bars + 15;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  int* abort_flag = reinterpret_cast<int*>(smem + C::kMiscOff + 4);
 
+  const int b = blockIdx.z, h = blockIdx.y, kt = blockIdx.x;
   int len, row0, slab;
   long long out_base;
   if (p.cu != nullptr) {
@@ -121,30 +143,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   const int n_steps = n_t - q_first;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bar_kv, 1);
-    mbar_init(&bar_qf, 1);
-    mbar_init(&bar_qe, 1);
-    mbar_init(&bar_of, 1);
-    mbar_init(&bar_oe, 1);
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_dp, 1);
-    mbar_init(&bar_p, 8);
-    mbar_init(&bar_ds, 8);
-    mbar_init(&bar_dq, 1);
-    mbar_init(&bar_dqfree, 8);
-    mbar_init(&bar_done, 1);
-    abort_flag = 0;
+    mbar_init(bar_kv, 1);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(bar_qf + st, 1);
+      mbar_init(bar_qe + st, 1);
+      mbar_init(bar_of + st, 1);
+      mbar_init(bar_oe + st, 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_p, 8);
+    mbar_init(bar_ds, 8);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_dqfree, 8);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&tmem_base_sh, 512);
+    tmem_alloc(tmem_base_sh, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
-  const WaitCtx w{&abort_flag, p.status, p.limit_ns};
+  const uint32_t tmem = *tmem_base_sh;
+  const WaitCtx w{abort_flag, p.status, p.limit_ns};
   float* s_l = reinterpret_cast<float*>(smem + C::kLOff);
   float* s_d = reinterpret_cast<float*>(smem + C::kDvOff);
 
@@ -153,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     setmaxnreg_inc<kComputeRegs>();
     const int ch = warp >> 2;        // query-column half
     const int quad = warp & 3;       // TMEM lanes 32*quad ..
-    const int j = quad * 32 + lane;  // key row within the tile (and query row for dQ)
+    const int j = quad * 32 + lane;  // this thread's TMEM lane: key row (and d or query row for dQ)
     const int key = kt * kBN + j;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + ch * 64;
@@ -162,8 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     bool ok = true;
     for (int k = 0; k < n_steps; ++k) {
       const int qi = q_first + k;
+      const int st = k & 1;
+      const float* sl = s_l + st * 128 + ch * 64;
+      const float* sd = s_d + st * 128 + ch * 64;
       // L / D of this query tile are visible once bar_qf completes; S^T once bar_s does
-      if (!warp_wait(&bar_qf, k & 1, w) || !warp_wait(&bar_s, k & 1, w)) {
+      if (!warp_wait(bar_qf + st, (k >> 1) & 1, w) || !warp_wait(bar_s, k & 1, w)) {
         ok = false;
         break;
       }
@@ -178,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       float pr[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float x = fmaf(__uint_as_float(sv[c >> 5][c & 31]), p.c2, -s_l[ch * 64 + c]);
+        const float x = fmaf(__uint_as_float(sv[c >> 5][c & 31]), p.c2, -sl[c]);
         float pv = ex2_approx(x);
         if (mask) {
           const int q = q0 + c;
@@ -196,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p);
+      if (lane == 0) mbar_arrive(bar_p);
 
-      if (!warp_wait(&bar_dp, k & 1, w)) {
+      if (!warp_wait(bar_dp, k & 1, w)) {
         ok = false;
         break;
       }
@@ -213,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c8 * 8 + 2 * e;
-          const float d0 = pr[c] * (__uint_as_float(sv[c >> 5][c & 31]) - s_d[ch * 64 + c]);
-          const float d1 = pr[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - s_d[ch * 64 + c + 1]);
+          const float d0 = pr[c] * (__uint_as_float(sv[c >> 5][c & 31]) - sd[c]);
+          const float d1 = pr[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - sd[c + 1]);
           u[e] = pack_bf16x2(d0, d1);
         }
         // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
@@ -223,16 +250,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_ds);
+      if (lane == 0) mbar_arrive(bar_ds);
 
-      // dQ_i rows (queries on lanes) into the float32 accumulator
-      if (!warp_wait(&bar_dq, k & 1, w)) {
+      // dQ of this query tile into the float32 accumulator
+      if (!warp_wait(bar_dq, k & 1, w)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      {
-        const int q = qi * kBM + j;  // this lane's query row
+      if constexpr (C::kDqTransposed) {
+        // dQ^T: lane j holds head-width column j for this half's 64 queries, so
+        // a warp's 32 reductions for one query cover 128 contiguous bytes.
+        tmem_ld32(tmem + lane_off + ch * 64, sv[0]);
+        tmem_ld32(tmem + lane_off + ch * 64 + 32, sv[1]);
+        tmem_ld_wait(sv[0]);
+        tmem_ld_wait(sv[1]);
+        float* dst = p.dq_acc + (out_base + q0) * D + j;
+        const int nq = min(64, len - q0);
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < nq) atomicAdd(dst + c * D, __uint_as_float(sv[c >> 5][c & 31]));
+      } else {
+        // dQ: lane j holds query row qi*128 + j, this half's D/2 columns
+        const int q = qi * kBM + j;
         float* dst = p.dq_acc + (out_base + q) * D + ch * (D / 2);
         const uint32_t t_dq = tmem + lane_off + ch * (D / 2);
 #pragma unroll 1
@@ -250,10 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dqfree);
+      if (lane == 0) mbar_arrive(bar_dqfree);
     }
     // epilogue: dV and dK rows of this CTA's keys
-    if (ok && warp_wait(&bar_done, 0, w)) {
+    if (ok && warp_wait(bar_done, 0, w)) {
       tc_fence_after();
       const bool row_ok = key < len;
 #pragma unroll 1
@@ -291,58 +331,62 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         tma_prefetch_desc(&p.tk);
         tma_prefetch_desc(&p.tv);
         tma_prefetch_desc(&p.tdo);
-        mbar_arrive_expect_tx(&bar_kv, 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
         for (int hf = 0; hf < C::kHalves; ++hf) {
-          tma_load_3d(smem + C::kKOff + hf * C::kHalfBytes, &p.tk, &bar_kv, hf * 64, row0 + kt * kBN, slab);
-          tma_load_3d(smem + C::kVOff + hf * C::kHalfBytes, &p.tv, &bar_kv, hf * 64, row0 + kt * kBN, slab);
+          tma_load_3d(smem + C::kKOff + hf * C::kHalfBytes, &p.tk, bar_kv, hf * 64, row0 + kt * kBN, slab);
+          tma_load_3d(smem + C::kVOff + hf * C::kHalfBytes, &p.tv, bar_kv, hf * 64, row0 + kt * kBN, slab);
         }
       }
       int issued = 0;
       for (int k = 0; k < n_steps; ++k) {
         const int qi = q_first + k;
-        // Q_i with its L and D values: the buffer is free once dK of the
-        // previous step (the last reader of Q, L and D) has completed.  Lane 0
-        // waits and the answer is broadcast, so the warp never splits.
+        const int st = k & 1;
+        // Stage st was last used by step k - 2; its Q / L / D are free once that
+        // step's dK (their last reader) has completed, its dO once that step's
+        // dV has.  Lane 0 waits and the answer is broadcast, so the warp never
+        // splits.
         int good = 1;
-        if (lane == 0 && k > 0) good = mbar_wait(&bar_qe, (k - 1) & 1, w);
+        if (lane == 0 && k >= 2) good = mbar_wait(bar_qe + st, ((k >> 1) - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = lane * 4 + e;
           const int qrow = qi * kBM + r;
           const bool in = qrow < len;
-          s_l[r] = in ? p.lse[out_base + qrow] * kLog2e : 0.f;
-          s_d[r] = in ? p.dvec[out_base + qrow] : 0.f;
+          s_l[st * 128 + r] = in ? p.lse[out_base + qrow] * kLog2e : 0.f;
+          s_d[st * 128 + r] = in ? p.dvec[out_base + qrow] : 0.f;
         }
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_qf, C::kTileBytes);
+          mbar_arrive_expect_tx(bar_qf + st, C::kTileBytes);
           for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(smem + C::kQOff + hf * C::kHalfBytes, &p.tq, &bar_qf, hf * 64, row0 + qi * kBM, slab);
+            tma_load_3d(smem + C::kQOff + st * C::kTileBytes + hf * C::kHalfBytes, &p.tq, bar_qf + st, hf * 64,
+                        row0 + qi * kBM, slab);
         }
-        // dO_i: free once dV of the previous step has completed
-        if (lane == 0 && k > 0) good = mbar_wait(&bar_oe, (k - 1) & 1, w);
+        if (lane == 0 && k >= 2) good = mbar_wait(bar_oe + st, ((k >> 1) - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_of, C::kTileBytes);
+          mbar_arrive_expect_tx(bar_of + st, C::kTileBytes);
           for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(smem + C::kDOOff + hf * C::kHalfBytes, &p.tdo, &bar_of, hf * 64, row0 + qi * kBM, slab);
+            tma_load_3d(smem + C::kDOOff + st * C::kTileBytes + hf * C::kHalfBytes, &p.tdo, bar_of + st,
+                        hf * 64, row0 + qi * kBM, slab);
         }
         issued = k + 1;
       }
-      if (lane == 0 && abort_flag) {
+      if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
-        mbar_wait_drain(&bar_kv, 0, p.limit_ns);
-        if (issued > 0) {
-          mbar_wait_drain(&bar_qf, (issued - 1) & 1, p.limit_ns);
-          mbar_wait_drain(&bar_of, (issued - 1) & 1, p.limit_ns);
+        mbar_wait_drain(bar_kv, 0, p.limit_ns);
+        for (int k = max(0, issued - 2); k < issued; ++k) {
+          mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
+          mbar_wait_drain(bar_of + (k & 1), (k >> 1) & 1, p.limit_ns);
         }
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t id_nn = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK: A K-major, B MN-major
-      const uint32_t id_dq = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
+      // dQ^T = K^T dS^T (M = D) or dQ = dS K (N = D): A and B both MN-major
+      const uint32_t id_dq = C::kDqTransposed ? idesc_bf16(128, 128, true, true) : idesc_bf16(128, D, true, true);
       const uint32_t sk = smem_u32(smem + C::kKOff), sv = smem_u32(smem + C::kVOff);
       const uint32_t sq = smem_u32(smem + C::kQOff), sdo = smem_u32(smem + C::kDOOff);
       const uint32_t sds = smem_u32(smem + C::kDSOff);
@@ -353,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       const uint64_t kDS = sdesc_sw128(sds, 16, 1024);
       const uint64_t mQ = sdesc_sw128(sq, C::kHalfBytes, 1024), mDO = sdesc_sw128(sdo, C::kHalfBytes, 1024);
       const uint64_t mK = sdesc_sw128(sk, C::kHalfBytes, 1024), mDS = sdesc_sw128(sds, C::kHalfBytes, 1024);
+      constexpr uint32_t kStageDesc = C::kTileBytes >> 4;
       // X^T = A B^T over the head width: A, B both [128 rows][D] K-major
       auto issue_nn = [&](uint32_t d_col, uint64_t a, uint64_t bb) {
 #pragma unroll 1
@@ -361,49 +406,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           mma_ss(tmem + d_col, a + off, bb + off, id_nn, ks > 0 ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&bar_kv, 0, w);
+      bool ok = mbar_wait(bar_kv, 0, w);
       for (int k = 0; ok && k < n_steps; ++k) {
+        const int st = k & 1;
         const uint32_t acc0 = k > 0 ? 1u : 0u;
-        if (!mbar_wait(&bar_qf, k & 1, w) || !mbar_wait(&bar_of, k & 1, w)) break;
+        if (!mbar_wait(bar_qf + st, (k >> 1) & 1, w) || !mbar_wait(bar_of + st, (k >> 1) & 1, w)) break;
         tc_fence_after();
         // dP^T = V dO^T: its columns were consumed before the previous dS was published
-        issue_nn(128, kV, kDO);
-        mma_commit(&bar_dp);
+        issue_nn(128, kV, kDO + st * kStageDesc);
+        mma_commit(bar_dp);
         // S^T = K Q^T into the columns the previous dQ used, once it is drained
         if (k > 0) {
-          if (!mbar_wait(&bar_dqfree, (k - 1) & 1, w)) break;
+          if (!mbar_wait(bar_dqfree, (k - 1) & 1, w)) break;
           tc_fence_after();
         }
-        issue_nn(0, kK, kQ);
-        mma_commit(&bar_s);
+        issue_nn(0, kK, kQ + st * kStageDesc);
+        mma_commit(bar_s);
         // dV += P^T dO: P^T (bf16) in TMEM, columns [0,32) for queries 0-63 and
         // [64,96) for queries 64-127; dO MN-major
-        if (!mbar_wait(&bar_p, k & 1, w)) break;
+        if (!mbar_wait(bar_p, k & 1, w)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t a_col = (ks >> 2) * 64 + (ks & 3) * 8;
-          mma_ts(tmem + 256, tmem + a_col, mDO + ((ks * 2048) >> 4), id_acc, (acc0 | (ks > 0)) ? 1u : 0u);
+          mma_ts(tmem + 256, tmem + a_col, mDO + st * kStageDesc + ((ks * 2048) >> 4), id_acc,
+                 (acc0 | (ks > 0)) ? 1u : 0u);
         }
-        mma_commit(&bar_oe);
+        mma_commit(bar_oe + st);
         // dK += dS^T Q: dS^T K-major from shared memory, Q MN-major
-        if (!mbar_wait(&bar_ds, k & 1, w)) break;
+        if (!mbar_wait(bar_ds, k & 1, w)) break;
         tc_fence_after();
 #pragma unroll 1
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + 384, kDS + off, mQ + ((ks * 2048) >> 4), id_acc, (acc0 | (ks > 0)) ? 1u : 0u);
+          mma_ss(tmem + 384, kDS + off, mQ + st * kStageDesc + ((ks * 2048) >> 4), id_acc,
+                 (acc0 | (ks > 0)) ? 1u : 0u);
         }
-        mma_commit(&bar_qe);
-        // dQ_i = dS K: the same dS buffer read MN-major (queries contiguous), K MN-major
+        mma_commit(bar_qe + st);
+        // dQ over the 128 keys (K = 16 keys per MMA): the dS buffer read MN-major
+        // (queries contiguous) and K read MN-major (head width contiguous)
 #pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + 0, mDS + ((ks * 2048) >> 4), mK + ((ks * 2048) >> 4), id_dq, ks > 0 ? 1u : 0u);
-        mma_commit(&bar_dq);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t a = C::kDqTransposed ? mK : mDS;
+          const uint64_t bb = C::kDqTransposed ? mDS : mK;
+          mma_ss(tmem + 0, a + ((ks * 2048) >> 4), bb + ((ks * 2048) >> 4), id_dq, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_dq);
       }
       // every MMA issued must be complete before tensor memory is released
-      mma_commit(&bar_done);
-      mbar_wait_drain(&bar_done, 0, p.limit_ns);
+      mma_commit(bar_done);
+      mbar_wait_drain(bar_done, 0, p.limit_ns);
     }
   }
 

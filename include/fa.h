@@ -165,7 +165,8 @@ const char* fa_strerror(fa_status status);
  * kernel status: FA_OK, FA_ERR_TIMEOUT (a bounded wait inside a kernel ran
  * out; the kernel stopped its work, released its tensor memory and returned)
  * or FA_ERR_INVALID (malformed cu_seqlens seen on the device).  Returns
- * FA_ERR_CUDA if the synchronisation itself fails.
+ * FA_ERR_CUDA if the synchronisation itself fails, or if a kernel found its
+ * launch environment unusable (it then skipped its work).
  */
 fa_status fa_get_last_device_error(void* stream);
 
