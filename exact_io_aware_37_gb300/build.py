@@ -21,15 +21,16 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
-SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_static_ws.cu"]
+SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_tc_bwd128.cu", "fa_static_ws.cu"]
 
-# The tensor-core kernels launch 384 threads and then move registers between
-# warpgroups with setmaxnreg (224 + 224 + 56 per thread).  That split is only
-# safe when every thread starts with 168 registers; a kernel that ptxas
-# compiled with fewer would wait forever in setmaxnreg.inc, so the build
-# refuses it.
-SPLIT_KERNELS = ("tc_fwd_kernel", "tc_bwd_kernel")
-SPLIT_LAUNCH_REGS = 168
+# The tensor-core kernels move registers between warpgroups with setmaxnreg
+# (384-thread kernels: 224 + 224 + 56 per thread from 168 at launch; the
+# 512-thread backward: 200 + 200 + 56 + 56 from 128).  Each split is only safe
+# when every thread starts with the launch count it was sized for; a kernel
+# that ptxas compiled with fewer would wait forever in setmaxnreg.inc, so the
+# build refuses it.
+# kernel name -> registers per thread it must be compiled with (checked in order)
+SPLIT_KERNELS = {"tc_bwd128_kernel": 128, "tc_fwd_kernel": 168, "tc_bwd_kernel": 168}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
@@ -58,8 +59,8 @@ def up_to_date():
 
 
 def check_register_split(log_text, src):
-    """Raise unless every split kernel in a ptxas -v log uses SPLIT_LAUNCH_REGS;
-    returns how many such kernels the log reports."""
+    """Raise unless every split kernel in a ptxas -v log uses its expected
+    register count; returns how many such kernels the log reports."""
     current = None
     seen = 0
     for line in log_text.splitlines():
@@ -68,11 +69,12 @@ def check_register_split(log_text, src):
             current = m.group(1)
             continue
         m = re.search(r"Used (\d+) registers", line)
-        if m and current and any(k in current for k in SPLIT_KERNELS):
+        name = next((k for k in SPLIT_KERNELS if current and k in current), None)
+        if m and name:
             regs = int(m.group(1))
-            if regs != SPLIT_LAUNCH_REGS:
+            if regs != SPLIT_KERNELS[name]:
                 raise RuntimeError(f"{src}: {current} compiled with {regs} registers; the warpgroup register "
-                                   f"split needs exactly {SPLIT_LAUNCH_REGS}")
+                                   f"split needs exactly {SPLIT_KERNELS[name]}")
             seen += 1
             current = None
     return seen

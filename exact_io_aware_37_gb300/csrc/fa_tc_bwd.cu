@@ -503,6 +503,13 @@ cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   note_launches(1);
   e = note_error("backward launch", cudaGetLastError());
   if (e != cudaSuccess) return e;
+  return launch_dq_convert(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s) {
+  const int D = p.D;
   const long long n4 = p.rows() * D / 4;
   const long long want = (n4 + 255) / 256;
   const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
@@ -512,11 +519,13 @@ cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   return note_error("dq convert launch", cudaGetLastError());
 }
 
-}  // namespace
 
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s) {
   if (p.D == 64) return launch_bwd_d<64>(p, s);
-  if (p.D == 128) return launch_bwd_d<128>(p, s);
+  if (p.D == 128) {
+    const cudaError_t e = launch_tc_bwd128(p, s);
+    return e == cudaSuccess ? launch_dq_convert(p, s) : e;
+  }
   return cudaErrorInvalidValue;
 }
 

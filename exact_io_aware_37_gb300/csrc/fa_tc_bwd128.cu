@@ -1,0 +1,462 @@
+// Tensor-core backward kernel for head width 128 (sm_103a, bf16 in, fp32
+// accumulate).
+//
+// Same method as the D = 64 kernel (tensortonic.com "FlashAttention",
+// section 7: every weight is rebuilt as P_ij = exp(s_ij - L_i) from the
+// saved log-sum-exp; dV = P^T dO, dS = P o (dO V^T - D), dK = scale dS^T Q,
+// dQ = scale dS K): a CTA owns one 128-key tile of K and V in shared memory
+// and visits the 128-query tiles that can see it.  All five products are
+// tcgen05 MMAs with M = N = 128:
+//     S^T  = K Q^T        -> TMEM [0,128)    (keys on lanes, queries on columns)
+//     dP^T = V dO^T       -> TMEM [128,256)
+//     dV  += P^T dO       (P^T in TMEM)  -> [256,384)
+//     dK  += dS^T Q       (dS^T in shared memory) -> [384,512)
+//     dQ^T = K^T dS^T     -> TMEM [0,128)    (head width on lanes), once P^T is used
+// Differences from the D = 64 kernel, which keep the per-step chain short:
+//   - a fourth warpgroup drains dQ^T: it copies the tile from TMEM to a
+//     shared staging buffer in 32-query chunks and lets the copy engine add
+//     each chunk into the float32 accumulator (cp.reduce.async.bulk), so the
+//     compute warps issue no atomics and the next step's S^T waits only for
+//     the TMEM read-out;
+//   - the L / D vectors are read four at a time and the masked and unmasked
+//     softmax loops are separate.
+// Warp roles (16 warps): 0-3 and 4-7 compute P^T and dS^T for query columns
+// [0,64) and [64,128); 8 = TMA / L / D producer; 9 = MMA issuer; 10-11 idle;
+// 12-15 drain dQ.  Registers: 128 per thread at launch, then 200 for the two
+// compute warpgroups and 56 for the others (setmaxnreg).
+#include <math.h>
+
+#include "fa_internal.cuh"
+#include "fa_tmap.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;
+constexpr int kTile = 128;  // keys per CTA and queries per step
+constexpr int kThreads = 512;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDrainWarp0 = 12;
+constexpr int kLaunchRegs4 = 128;
+constexpr int kComputeRegs4 = 200;
+constexpr int kOtherRegs4 = 56;
+static_assert(2 * 128 * kComputeRegs4 + 2 * 128 * kOtherRegs4 <= kThreads * kLaunchRegs4,
+              "register split exceeds the launch budget");
+
+struct Bwd128Params {
+  CUtensorMap tq, tk, tv, tdo;
+  const float* lse;
+  const float* dvec;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const int32_t* cu;
+  unsigned* status;
+  unsigned long long limit_ns;
+  int B, H, N, T;
+  float c2;  // scale * log2(e)
+  float scale;
+  int causal;
+};
+
+// Shared memory, dynamic only (1024-byte aligned base, checked).
+constexpr int kTileBytes = kTile * D * 2;  // 32 KB
+constexpr int kHalfBytes = kTile * 128;    // 16 KB: 64 columns of 128 rows
+constexpr int kKOff = 0;
+constexpr int kVOff = kTileBytes;
+constexpr int kQOff = 2 * kTileBytes;      // 2 stages
+constexpr int kDOOff = 4 * kTileBytes;     // 1 stage
+constexpr int kDSOff = 5 * kTileBytes;     // dS^T [128 keys][128 queries] bf16
+constexpr int kStageOff = 6 * kTileBytes;  // dQ staging: 2 buffers x [32 queries][128] fp32
+constexpr int kChunkQ = 32;
+constexpr int kChunkBytes = kChunkQ * D * 4;  // 16 KB
+constexpr int kLOff = kStageOff + 2 * kChunkBytes;  // 2 x 128 floats: L * log2(e)
+constexpr int kDvOff = kLOff + 1024;                // 2 x 128 floats: D
+constexpr int kBarOff = kDvOff + 1024;
+constexpr int kNumBars = 16;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kSmemBytes = kMiscOff + 16;
+static_assert(kSmemBytes <= 232448, "shared-memory budget");
+
+__global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_constant__ Bwd128Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (smem_u32(smem) & 1023u) {  // the swizzled tile layout needs a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicOr(p.status, kDevInternal);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* bar_kv = bars + 0;      // K, V loaded
+  uint64_t* bar_qf = bars + 1;      // [2] Q tile + L / D of a stage loaded
+  uint64_t* bar_qe = bars + 3;      // [2] Q / L / D stage free (dK done)
+  uint64_t* bar_of = bars + 5;      // dO tile loaded
+  uint64_t* bar_oe = bars + 6;      // dO buffer free (dV done)
+  uint64_t* bar_s = bars + 7;       // S^T ready
+  uint64_t* bar_dp = bars + 8;      // dP^T ready
+  uint64_t* bar_p = bars + 9;       // P^T written (8 compute warps)
+  uint64_t* bar_ds = bars + 10;     // dS^T written (8 compute warps)
+  uint64_t* bar_dq = bars + 11;     // dQ^T ready
+  uint64_t* bar_dqfree = bars + 12; // dQ^T read out of TMEM (4 drain warps)
+  uint64_t* bar_done = bars + 13;   // every MMA complete
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+  int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
+  float* s_l = reinterpret_cast<float*>(smem + kLOff);
+  float* s_d = reinterpret_cast<float*>(smem + kDvOff);
+
+  const int b = blockIdx.z, h = blockIdx.y, kt = blockIdx.x;
+  int len, row0, slab;
+  long long out_base;
+  if (p.cu != nullptr) {
+    const int s0 = p.cu[b], s1 = p.cu[b + 1];
+    if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
+      if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
+      return;
+    }
+    len = s1 - s0;
+    row0 = s0;
+    slab = h;
+    out_base = (long long)h * p.T + s0;
+  } else {
+    len = p.N;
+    row0 = 0;
+    slab = b * p.H + h;
+    out_base = (long long)slab * p.N;
+  }
+  const int n_t = (len + kTile - 1) / kTile;
+  if (kt >= n_t) return;
+  const int q_first = p.causal ? kt : 0;  // earlier query tiles never see these keys
+  const int n_steps = n_t - q_first;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint64_t* bar = bars + i;
+      mbar_init(bar, (bar == bar_p || bar == bar_ds) ? 8 : (bar == bar_dqfree ? 4 : 1));
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_sh;
+  const WaitCtx w{abort_flag, p.status, p.limit_ns};
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ P^T, dS^T, epilogue
+    setmaxnreg_inc<kComputeRegs4>();
+    const int ch = warp >> 2;        // query-column half
+    const int quad = warp & 3;       // TMEM lanes 32*quad ..
+    const int j = quad * 32 + lane;  // key row within the tile
+    const int key = kt * kTile + j;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + ch * 64;
+    const uint32_t t_dp = tmem + lane_off + 128 + ch * 64;
+    uint8_t* ds_row = smem + kDSOff + ch * kHalfBytes + (j >> 3) * 1024 + (j & 7) * 128;
+    bool ok = true;
+    for (int k = 0; k < n_steps; ++k) {
+      const int qi = q_first + k;
+      const int st = k & 1;
+      const float4* sl4 = reinterpret_cast<const float4*>(s_l + st * 128 + ch * 64);
+      const float4* sd4 = reinterpret_cast<const float4*>(s_d + st * 128 + ch * 64);
+      if (!warp_wait(bar_qf + st, (k >> 1) & 1, w) || !warp_wait(bar_s, k & 1, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[2][32];
+      tmem_ld32(t_s, sv[0]);
+      tmem_ld32(t_s + 32, sv[1]);
+      tmem_ld_wait(sv[0]);
+      tmem_ld_wait(sv[1]);
+      const int q0 = qi * kTile + ch * 64;  // first query (within the sequence) of this half
+      float pr[64];
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = sl4[c4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          pr[c] = ex2_approx(fmaf(__uint_as_float(sv[c >> 5][c & 31]), p.c2, -lv[e]));
+        }
+      }
+      if ((p.causal && qi == kt) || (kt * kTile + kTile > len) || (qi * kTile + kTile > len)) {
+        // diagonal or ragged tile: weights of future keys, padding keys and padding queries are zero
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int q = q0 + c;
+          if (q >= len || key >= len || (p.causal && key > q)) pr[c] = 0.f;
+        }
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        tmem_st32(t_s, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+
+      if (!warp_wait(bar_dp, k & 1, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_ld32(t_dp, sv[0]);
+      tmem_ld32(t_dp + 32, sv[1]);
+      tmem_ld_wait(sv[0]);
+      tmem_ld_wait(sv[1]);
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const float4 da = sd4[2 * c8], db = sd4[2 * c8 + 1];
+        const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+        uint32_t u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c8 * 8 + 2 * e;
+          const float d0 = pr[c] * (__uint_as_float(sv[c >> 5][c & 31]) - dv[2 * e]);
+          const float d1 = pr[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - dv[2 * e + 1]);
+          u[e] = pack_bf16x2(d0, d1);
+        }
+        // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
+        *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
+    }
+    // epilogue: dV and dK rows of this CTA's keys
+    if (ok && warp_wait(bar_done, 0, w)) {
+      tc_fence_after();
+      const bool row_ok = key < len;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + (out_base + key) * D + ch * 64;
+        const float mul = which == 0 ? 1.f : p.scale;
+        const uint32_t t_acc = tmem + lane_off + (which == 0 ? 256 : 384) + ch * 64;
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(t_acc + c, v);
+          tmem_ld_wait(v);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+              u.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+              u.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+              u.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+              dst[v4] = u;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp >= kDrainWarp0) {
+    // ------------------------------------------------------------ dQ drain
+    setmaxnreg_dec<kOtherRegs4>();
+    const int quad = warp & 3;
+    const int d = quad * 32 + lane;  // TMEM lane = head-width column of dQ^T
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const bool leader = warp == kDrainWarp0 && lane == 0;
+    int g = 0;  // chunks issued so far (buffer = g & 1)
+    for (int k = 0; k < n_steps; ++k) {
+      const int q0 = (q_first + k) * kTile;
+      // the four drain warps decide together (they meet at named barriers below)
+      if (!named_bar_and(1, 128, warp_wait(bar_dq, k & 1, w))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kTile / kChunkQ; ++c, ++g) {
+        float* buf = reinterpret_cast<float*>(smem + kStageOff + (g & 1) * kChunkBytes);
+        // the buffer's previous chunk (issued two chunks ago) must have been read
+        if (leader && g >= 2) bulk_wait_read<1>();
+        named_bar_sync(1, 128);
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + c * kChunkQ, v);
+        tmem_ld_wait(v);
+        if (c == kTile / kChunkQ - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dqfree);  // all of dQ^T is now in registers or staged
+        }
+#pragma unroll
+        for (int e = 0; e < kChunkQ; ++e) buf[e * D + d] = __uint_as_float(v[e]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          const int nq = min(kChunkQ, len - (q0 + c * kChunkQ));
+          if (nq > 0) bulk_reduce_add_f32(p.dq_acc + (out_base + q0 + c * kChunkQ) * D, buf, (uint32_t)nq * D * 4);
+          bulk_commit();
+        }
+      }
+    }
+    if (leader) bulk_wait_all();
+  } else {
+    setmaxnreg_dec<kOtherRegs4>();
+    if (warp == kTmaWarp) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        tma_prefetch_desc(&p.tq);
+        tma_prefetch_desc(&p.tk);
+        tma_prefetch_desc(&p.tv);
+        tma_prefetch_desc(&p.tdo);
+        mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_3d(smem + kKOff + hf * kHalfBytes, &p.tk, bar_kv, hf * 64, row0 + kt * kTile, slab);
+          tma_load_3d(smem + kVOff + hf * kHalfBytes, &p.tv, bar_kv, hf * 64, row0 + kt * kTile, slab);
+        }
+      }
+      int issued = 0;
+      for (int k = 0; k < n_steps; ++k) {
+        const int qi = q_first + k;
+        const int st = k & 1;
+        // Q / L / D stage st was last used by step k - 2 (free once its dK has
+        // completed); the single dO buffer by step k - 1 (free once its dV has).
+        // Lane 0 waits and the answer is broadcast, so the warp never splits.
+        int good = 1;
+        if (lane == 0 && k >= 2) good = mbar_wait(bar_qe + st, ((k >> 1) - 1) & 1, w);
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = lane * 4 + e;
+          const int qrow = qi * kTile + r;
+          const bool in = qrow < len;
+          s_l[st * 128 + r] = in ? p.lse[out_base + qrow] * kLog2e : 0.f;
+          s_d[st * 128 + r] = in ? p.dvec[out_base + qrow] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_qf + st, kTileBytes);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
+                        row0 + qi * kTile, slab);
+        }
+        if (lane == 0 && k >= 1) good = mbar_wait(bar_oe, (k - 1) & 1, w);
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_of, kTileBytes);
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, row0 + qi * kTile, slab);
+        }
+        issued = k + 1;
+      }
+      if (lane == 0 && *abort_flag) {
+        // let copies already in flight land before the CTA's memory is released
+        mbar_wait_drain(bar_kv, 0, p.limit_ns);
+        if (issued > 0) mbar_wait_drain(bar_of, (issued - 1) & 1, p.limit_ns);
+        for (int k = max(0, issued - 2); k < issued; ++k)
+          mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
+      }
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t id_nn = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
+      const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK: B MN-major
+      const uint32_t id_dq = idesc_bf16(128, 128, true, true);    // dQ^T: both MN-major
+      // Descriptors, advanced by adding (byte offset >> 4) to the start field.
+      // k* = K-major view, m* = MN-major view of the same tile.
+      const uint64_t kK = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);
+      const uint64_t kV = sdesc_sw128(smem_u32(smem + kVOff), 16, 1024);
+      const uint64_t mK = sdesc_sw128(smem_u32(smem + kKOff), kHalfBytes, 1024);
+      const uint64_t kQ = sdesc_sw128(smem_u32(smem + kQOff), 16, 1024);
+      const uint64_t mQ = sdesc_sw128(smem_u32(smem + kQOff), kHalfBytes, 1024);
+      const uint64_t kDO = sdesc_sw128(smem_u32(smem + kDOOff), 16, 1024);
+      const uint64_t mDO = sdesc_sw128(smem_u32(smem + kDOOff), kHalfBytes, 1024);
+      const uint64_t kDS = sdesc_sw128(smem_u32(smem + kDSOff), 16, 1024);
+      const uint64_t mDS = sdesc_sw128(smem_u32(smem + kDSOff), kHalfBytes, 1024);
+      constexpr uint32_t kStageDesc = kTileBytes >> 4;
+      auto koff = [](int ks) { return (uint32_t)(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4); };
+      auto moff = [](int ks) { return (uint32_t)((ks * 2048) >> 4); };
+      bool ok = mbar_wait(bar_kv, 0, w);
+      for (int k = 0; ok && k < n_steps; ++k) {
+        const int st = k & 1;
+        const uint32_t acc0 = k > 0 ? 1u : 0u;
+        // S^T = K Q^T into the columns the previous dQ^T used, once drained
+        if (!mbar_wait(bar_qf + st, (k >> 1) & 1, w)) break;
+        if (k > 0 && !mbar_wait(bar_dqfree, (k - 1) & 1, w)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + 0, kK + koff(ks), kQ + st * kStageDesc + koff(ks), id_nn, ks > 0 ? 1u : 0u);
+        mma_commit(bar_s);
+        // dP^T = V dO^T: its columns were read before the previous dS^T was published
+        if (!mbar_wait(bar_of, k & 1, w)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tmem + 128, kV + koff(ks), kDO + koff(ks), id_nn, ks > 0 ? 1u : 0u);
+        mma_commit(bar_dp);
+        // dV += P^T dO: P^T (bf16) in TMEM columns [0,32) (queries 0-63) and [64,96)
+        if (!mbar_wait(bar_p, k & 1, w)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ts(tmem + 256, tmem + (ks >> 2) * 64 + (ks & 3) * 8, mDO + moff(ks), id_acc,
+                 (acc0 | (ks > 0)) ? 1u : 0u);
+        mma_commit(bar_oe);
+        // dK += dS^T Q, then dQ^T = K^T dS^T over the 128 keys
+        if (!mbar_wait(bar_ds, k & 1, w)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ss(tmem + 384, kDS + koff(ks), mQ + st * kStageDesc + moff(ks), id_acc, (acc0 | (ks > 0)) ? 1u : 0u);
+        mma_commit(bar_qe + st);
+#pragma unroll 1
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ss(tmem + 0, mK + moff(ks), mDS + moff(ks), id_dq, ks > 0 ? 1u : 0u);
+        mma_commit(bar_dq);
+      }
+      // every MMA issued must be complete before tensor memory is released
+      mma_commit(bar_done);
+      mbar_wait_drain(bar_done, 0, p.limit_ns);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
+  Bwd128Params bp;
+  if (!make_bf16_map(&bp.tq, p.q, p, kTile) || !make_bf16_map(&bp.tk, p.k, p, kTile) ||
+      !make_bf16_map(&bp.tv, p.v, p, kTile) || !make_bf16_map(&bp.tdo, p.dout, p, kTile))
+    return note_error("backward tensor map encode", cudaErrorInvalidValue);
+  bp.lse = p.lse;
+  bp.dvec = p.dvec;
+  bp.dq_acc = p.dq_acc;
+  bp.dk = static_cast<__nv_bfloat16*>(p.dk);
+  bp.dv = static_cast<__nv_bfloat16*>(p.dv);
+  bp.cu = p.cu;
+  bp.status = p.status;
+  bp.limit_ns = p.wait_limit_ns;
+  bp.B = p.B;
+  bp.H = p.H;
+  bp.N = p.N;
+  bp.T = p.T;
+  bp.c2 = p.scale * kLog2e;
+  bp.scale = p.scale;
+  bp.causal = p.causal;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return note_error("backward smem attribute", e);
+  dim3 grid((p.N + kTile - 1) / kTile, p.H, p.B);
+  tc_bwd128_kernel<<<grid, kThreads, kSmemBytes, s>>>(bp);
+  note_launches(1);
+  return note_error("backward launch", cudaGetLastError());
+}
+
+}  // namespace fa
