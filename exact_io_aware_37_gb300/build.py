@@ -24,8 +24,8 @@ LIB_PATH = os.path.join(BUILD, LIB_NAME)
 SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_tc_bwd128.cu", "fa_static_ws.cu"]
 
 # The tensor-core kernels move registers between warpgroups with setmaxnreg
-# (384-thread kernels: 224 + 224 + 56 per thread from 168 at launch; the
-# 512-thread backward: 200 + 200 + 56 + 56 from 128).  Each split is only safe
+# (384-thread kernels: 200 + 200 + 104 per thread from 168 at launch; the
+# 512-thread backward: 176 + 176 + 104 + 56 from 128).  Each split is only safe
 # when every thread starts with the launch count it was sized for; a kernel
 # that ptxas compiled with fewer would wait forever in setmaxnreg.inc, so the
 # build refuses it.

@@ -398,12 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       const uint64_t mQ = sdesc_sw128(sq, C::kHalfBytes, 1024), mDO = sdesc_sw128(sdo, C::kHalfBytes, 1024);
       const uint64_t mK = sdesc_sw128(sk, C::kHalfBytes, 1024), mDS = sdesc_sw128(sds, C::kHalfBytes, 1024);
       constexpr uint32_t kStageDesc = C::kTileBytes >> 4;
-      // X^T = A B^T over the head width: A, B both [128 rows][D] K-major
-      auto issue_nn = [&](uint32_t d_col, uint64_t a, uint64_t bb) {
-#pragma unroll 1
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + d_col, a + off, bb + off, id_nn, ks > 0 ? 1u : 0u);
+      // X^T = A B^T over the head width: A, B both [128 rows][D] K-major,
+      // D/16 MMAs issued back to back
+      auto issue_nn = [&](uint32_t d_col, uint64_t a0, uint64_t b0) {
+        if constexpr (D == 128) {
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
+            a[ks] = a0 + off;
+            b[ks] = b0 + off;
+          }
+          mma_ss_x8(tmem + d_col, a, b, id_nn, 0u);
+        } else {
+          uint64_t a[4], b[4];
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            a[ks] = a0 + ks * 2;
+            b[ks] = b0 + ks * 2;
+          }
+          mma_ss_x4(tmem + d_col, a, b, id_nn, 0u);
         }
       };
       bool ok = mbar_wait(bar_kv, 0, w);
@@ -426,30 +440,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // [64,96) for queries 64-127; dO MN-major
         if (!mbar_wait(bar_p, k & 1, w)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t a_col = (ks >> 2) * 64 + (ks & 3) * 8;
-          mma_ts(tmem + 256, tmem + a_col, mDO + st * kStageDesc + ((ks * 2048) >> 4), id_acc,
-                 (acc0 | (ks > 0)) ? 1u : 0u);
+        {
+          uint32_t at[8];
+          uint64_t b[8];
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            at[ks] = tmem + (ks >> 2) * 64 + (ks & 3) * 8;
+            b[ks] = mDO + st * kStageDesc + ((ks * 2048) >> 4);
+          }
+          mma_ts_x8(tmem + 256, at, b, id_acc, acc0);
         }
         mma_commit(bar_oe + st);
         // dK += dS^T Q: dS^T K-major from shared memory, Q MN-major
         if (!mbar_wait(bar_ds, k & 1, w)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + 384, kDS + off, mQ + st * kStageDesc + ((ks * 2048) >> 4), id_acc,
-                 (acc0 | (ks > 0)) ? 1u : 0u);
+        {
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            a[ks] = kDS + (((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4);
+            b[ks] = mQ + st * kStageDesc + ((ks * 2048) >> 4);
+          }
+          mma_ss_x8(tmem + 384, a, b, id_acc, acc0);
         }
         mma_commit(bar_qe + st);
         // dQ over the 128 keys (K = 16 keys per MMA): the dS buffer read MN-major
         // (queries contiguous) and K read MN-major (head width contiguous)
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t a = C::kDqTransposed ? mK : mDS;
-          const uint64_t bb = C::kDqTransposed ? mDS : mK;
-          mma_ss(tmem + 0, a + ((ks * 2048) >> 4), bb + ((ks * 2048) >> 4), id_dq, ks > 0 ? 1u : 0u);
+        {
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            a[ks] = (C::kDqTransposed ? mK : mDS) + ((ks * 2048) >> 4);
+            b[ks] = (C::kDqTransposed ? mDS : mK) + ((ks * 2048) >> 4);
+          }
+          mma_ss_x8(tmem + 0, a, b, id_dq, 0u);
         }
         mma_commit(bar_dq);
       }

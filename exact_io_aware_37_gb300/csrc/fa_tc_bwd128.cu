@@ -6,24 +6,27 @@
 // saved log-sum-exp; dV = P^T dO, dS = P o (dO V^T - D), dK = scale dS^T Q,
 // dQ = scale dS K): a CTA owns one 128-key tile of K and V in shared memory
 // and visits the 128-query tiles that can see it.  All five products are
-// tcgen05 MMAs with M = N = 128:
-//     S^T  = K Q^T        -> TMEM [0,128)    (keys on lanes, queries on columns)
-//     dP^T = V dO^T       -> TMEM [128,256)
-//     dV  += P^T dO       (P^T in TMEM)  -> [256,384)
-//     dK  += dS^T Q       (dS^T in shared memory) -> [384,512)
-//     dQ^T = K^T dS^T     -> TMEM [0,128)    (head width on lanes), once P^T is used
-// Differences from the D = 64 kernel, which keep the per-step chain short:
-//   - a fourth warpgroup drains dQ^T: it copies the tile from TMEM to a
-//     shared staging buffer in 32-query chunks and lets the copy engine add
-//     each chunk into the float32 accumulator (cp.reduce.async.bulk), so the
-//     compute warps issue no atomics and the next step's S^T waits only for
-//     the TMEM read-out;
-//   - the L / D vectors are read four at a time and the masked and unmasked
-//     softmax loops are separate.
+// tcgen05 MMAs with M = N = 128, placed in tensor memory as
+//     [0,128)   S^T = K Q^T, then P^T (bf16) over its columns [0,32) and [64,96)
+//     [128,256) dP^T = V dO^T, then dS^T (bf16) over [128,160) and [192,224),
+//               then dQ^T = K^T dS^T (head width on lanes)
+//     [256,384) dV += P^T dO        (A = P^T from tensor memory)
+//     [384,512) dK += dS^T Q        (A = dS^T from tensor memory)
+// dQ^T also needs dS^T as an MN-major shared-memory operand, so the compute
+// warps write it to both places.  The MMA order per step k is
+//     dV_k, S^T_{k+1}, dK_k, dQ^T_k, [dQ^T_k drained] dP^T_{k+1}
+// so the next step's P^T is built while dK, dQ and the drain of this step
+// run.  Shared-memory operand traffic is the limit of this formulation
+// (two SS products of 8 KB per 64-cycle MMA besides the TS ones), which is
+// why everything that can be read from tensor memory is.
+//
 // Warp roles (16 warps): 0-3 and 4-7 compute P^T and dS^T for query columns
 // [0,64) and [64,128); 8 = TMA / L / D producer; 9 = MMA issuer; 10-11 idle;
-// 12-15 drain dQ.  Registers: 128 per thread at launch, then 200 for the two
-// compute warpgroups and 56 for the others (setmaxnreg).
+// 12-15 drain dQ^T from tensor memory into the float32 accumulator with
+// reductions whose 32 lanes cover one contiguous 128-byte line.
+// Registers: 128 per thread at launch, then 176 for the two compute
+// warpgroups, 104 for the producer / MMA warpgroup and 56 for the drain
+// warpgroup (setmaxnreg).
 #include <math.h>
 
 #include "fa_internal.cuh"
@@ -42,9 +45,10 @@ constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDrainWarp0 = 12;
 constexpr int kLaunchRegs4 = 128;
-constexpr int kComputeRegs4 = 200;
-constexpr int kOtherRegs4 = 56;
-static_assert(2 * 128 * kComputeRegs4 + 2 * 128 * kOtherRegs4 <= kThreads * kLaunchRegs4,
+constexpr int kComputeRegs4 = 176;
+constexpr int kSupportRegs4 = 104;  // producer / MMA warpgroup
+constexpr int kDrainRegs4 = 56;
+static_assert(2 * 128 * kComputeRegs4 + 128 * kSupportRegs4 + 128 * kDrainRegs4 <= kThreads * kLaunchRegs4,
               "register split exceeds the launch budget");
 
 struct Bwd128Params {
@@ -69,13 +73,10 @@ constexpr int kHalfBytes = kTile * 128;    // 16 KB: 64 columns of 128 rows
 constexpr int kKOff = 0;
 constexpr int kVOff = kTileBytes;
 constexpr int kQOff = 2 * kTileBytes;      // 2 stages
-constexpr int kDOOff = 4 * kTileBytes;     // 1 stage
-constexpr int kDSOff = 5 * kTileBytes;     // dS^T [128 keys][128 queries] bf16
-constexpr int kStageOff = 6 * kTileBytes;  // dQ staging: 2 buffers x [32 queries][128] fp32
-constexpr int kChunkQ = 32;
-constexpr int kChunkBytes = kChunkQ * D * 4;  // 16 KB
-constexpr int kLOff = kStageOff + 2 * kChunkBytes;  // 2 x 128 floats: L * log2(e)
-constexpr int kDvOff = kLOff + 1024;                // 2 x 128 floats: D
+constexpr int kDOOff = 4 * kTileBytes;     // 2 stages
+constexpr int kDSOff = 6 * kTileBytes;     // dS^T [128 keys][128 queries] bf16
+constexpr int kLOff = kDSOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
+constexpr int kDvOff = kLOff + 1024;        // 2 x 128 floats: D
 constexpr int kBarOff = kDvOff + 1024;
 constexpr int kNumBars = 16;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -93,15 +94,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_kv = bars + 0;      // K, V loaded
   uint64_t* bar_qf = bars + 1;      // [2] Q tile + L / D of a stage loaded
   uint64_t* bar_qe = bars + 3;      // [2] Q / L / D stage free (dK done)
-  uint64_t* bar_of = bars + 5;      // dO tile loaded
-  uint64_t* bar_oe = bars + 6;      // dO buffer free (dV done)
-  uint64_t* bar_s = bars + 7;       // S^T ready
-  uint64_t* bar_dp = bars + 8;      // dP^T ready
-  uint64_t* bar_p = bars + 9;       // P^T written (8 compute warps)
-  uint64_t* bar_ds = bars + 10;     // dS^T written (8 compute warps)
-  uint64_t* bar_dq = bars + 11;     // dQ^T ready
-  uint64_t* bar_dqfree = bars + 12; // dQ^T read out of TMEM (4 drain warps)
-  uint64_t* bar_done = bars + 13;   // every MMA complete
+  uint64_t* bar_of = bars + 5;      // [2] dO tile loaded
+  uint64_t* bar_oe = bars + 7;      // [2] dO stage free (dV done)
+  uint64_t* bar_s = bars + 9;       // S^T ready
+  uint64_t* bar_dp = bars + 10;     // dP^T ready
+  uint64_t* bar_p = bars + 11;      // P^T written (8 compute warps)
+  uint64_t* bar_ds = bars + 12;     // dS^T written (8 compute warps)
+  uint64_t* bar_dq = bars + 13;     // dQ^T ready
+  uint64_t* bar_dqfree = bars + 14; // dQ^T read out of TMEM (4 drain warps)
+  uint64_t* bar_done = bars + 15;   // every MMA complete
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
   float* s_l = reinterpret_cast<float*>(smem + kLOff);
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       tmem_ld32(t_dp + 32, sv[1]);
       tmem_ld_wait(sv[0]);
       tmem_ld_wait(sv[1]);
+      uint32_t dsp[32];
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         const float4 da = sd4[2 * c8], db = sd4[2 * c8 + 1];
@@ -230,8 +232,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         }
         // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
         *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+        dsp[4 * c8 + 0] = u[0];
+        dsp[4 * c8 + 1] = u[1];
+        dsp[4 * c8 + 2] = u[2];
+        dsp[4 * c8 + 3] = u[3];
       }
+      tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
       fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
@@ -267,45 +275,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     }
   } else if (warp >= kDrainWarp0) {
     // ------------------------------------------------------------ dQ drain
-    setmaxnreg_dec<kOtherRegs4>();
+    setmaxnreg_dec<kDrainRegs4>();
     const int quad = warp & 3;
     const int d = quad * 32 + lane;  // TMEM lane = head-width column of dQ^T
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const bool leader = warp == kDrainWarp0 && lane == 0;
-    int g = 0;  // chunks issued so far (buffer = g & 1)
+    const uint32_t t_dq = tmem + ((uint32_t)(quad * 32) << 16) + 128;
     for (int k = 0; k < n_steps; ++k) {
       const int q0 = (q_first + k) * kTile;
-      // the four drain warps decide together (they meet at named barriers below)
-      if (!named_bar_and(1, 128, warp_wait(bar_dq, k & 1, w))) break;
+      if (!warp_wait(bar_dq, k & 1, w)) break;
       tc_fence_after();
+      float* dst = p.dq_acc + (out_base + q0) * D + d;
 #pragma unroll 1
-      for (int c = 0; c < kTile / kChunkQ; ++c, ++g) {
-        float* buf = reinterpret_cast<float*>(smem + kStageOff + (g & 1) * kChunkBytes);
-        // the buffer's previous chunk (issued two chunks ago) must have been read
-        if (leader && g >= 2) bulk_wait_read<1>();
-        named_bar_sync(1, 128);
+      for (int c = 0; c < kTile / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + c * kChunkQ, v);
+        tmem_ld32(t_dq + c * 32, v);
         tmem_ld_wait(v);
-        if (c == kTile / kChunkQ - 1) {
+        if (c == kTile / 32 - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_dqfree);  // all of dQ^T is now in registers or staged
+          if (lane == 0) mbar_arrive(bar_dqfree);  // the whole tile is out of tensor memory
         }
+        const int nq = min(32, len - (q0 + c * 32));
 #pragma unroll
-        for (int e = 0; e < kChunkQ; ++e) buf[e * D + d] = __uint_as_float(v[e]);
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader) {
-          const int nq = min(kChunkQ, len - (q0 + c * kChunkQ));
-          if (nq > 0) bulk_reduce_add_f32(p.dq_acc + (out_base + q0 + c * kChunkQ) * D, buf, (uint32_t)nq * D * 4);
-          bulk_commit();
-        }
+        for (int e = 0; e < 32; ++e)
+          if (e < nq) atomicAdd(dst + (c * 32 + e) * D, __uint_as_float(v[e]));
       }
     }
-    if (leader) bulk_wait_all();
   } else {
-    setmaxnreg_dec<kOtherRegs4>();
+    setmaxnreg_dec<kSupportRegs4>();
     if (warp == kTmaWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
@@ -323,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       for (int k = 0; k < n_steps; ++k) {
         const int qi = q_first + k;
         const int st = k & 1;
-        // Q / L / D stage st was last used by step k - 2 (free once its dK has
-        // completed); the single dO buffer by step k - 1 (free once its dV has).
+        // stage st was last used by step k - 2: its Q / L / D are free once that
+        // step's dK has completed, its dO once that step's dV has.
         // Lane 0 waits and the answer is broadcast, so the warp never splits.
         int good = 1;
         if (lane == 0 && k >= 2) good = mbar_wait(bar_qe + st, ((k >> 1) - 1) & 1, w);
@@ -344,21 +340,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
             tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
                         row0 + qi * kTile, slab);
         }
-        if (lane == 0 && k >= 1) good = mbar_wait(bar_oe, (k - 1) & 1, w);
+        if (lane == 0 && k >= 2) good = mbar_wait(bar_oe + st, ((k >> 1) - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_of, kTileBytes);
+          mbar_arrive_expect_tx(bar_of + st, kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, row0 + qi * kTile, slab);
+            tma_load_3d(smem + kDOOff + st * kTileBytes + hf * kHalfBytes, &p.tdo, bar_of + st, hf * 64,
+                        row0 + qi * kTile, slab);
         }
         issued = k + 1;
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
         mbar_wait_drain(bar_kv, 0, p.limit_ns);
-        if (issued > 0) mbar_wait_drain(bar_of, (issued - 1) & 1, p.limit_ns);
-        for (int k = max(0, issued - 2); k < issued; ++k)
+        for (int k = max(0, issued - 2); k < issued; ++k) {
           mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
+          mbar_wait_drain(bar_of + (k & 1), (k >> 1) & 1, p.limit_ns);
+        }
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -374,49 +372,85 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       const uint64_t mQ = sdesc_sw128(smem_u32(smem + kQOff), kHalfBytes, 1024);
       const uint64_t kDO = sdesc_sw128(smem_u32(smem + kDOOff), 16, 1024);
       const uint64_t mDO = sdesc_sw128(smem_u32(smem + kDOOff), kHalfBytes, 1024);
-      const uint64_t kDS = sdesc_sw128(smem_u32(smem + kDSOff), 16, 1024);
       const uint64_t mDS = sdesc_sw128(smem_u32(smem + kDSOff), kHalfBytes, 1024);
       constexpr uint32_t kStageDesc = kTileBytes >> 4;
       auto koff = [](int ks) { return (uint32_t)(((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4); };
       auto moff = [](int ks) { return (uint32_t)((ks * 2048) >> 4); };
-      bool ok = mbar_wait(bar_kv, 0, w);
+      // Each group of 8 MMAs is issued back to back from one asm block.
+      uint64_t a[8], b[8];
+      uint32_t at[8];
+      auto issue_s = [&](int k) {  // S^T_k = K Q_k^T -> [0,128)
+        const int st = k & 1;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          a[ks] = kK + koff(ks);
+          b[ks] = kQ + st * kStageDesc + koff(ks);
+        }
+        mma_ss_x8(tmem + 0, a, b, id_nn, 0u);
+        mma_commit(bar_s);
+      };
+      auto issue_dp = [&](int k) {  // dP^T_k = V dO_k^T -> [128,256)
+        const int st = k & 1;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          a[ks] = kV + koff(ks);
+          b[ks] = kDO + st * kStageDesc + koff(ks);
+        }
+        mma_ss_x8(tmem + 128, a, b, id_nn, 0u);
+        mma_commit(bar_dp);
+      };
+      bool ok = mbar_wait(bar_kv, 0, w) && mbar_wait(bar_qf, 0, w);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = mbar_wait(bar_of, 0, w);
+        tc_fence_after();
+        if (ok) issue_dp(0);
+      }
       for (int k = 0; ok && k < n_steps; ++k) {
         const int st = k & 1;
         const uint32_t acc0 = k > 0 ? 1u : 0u;
-        // S^T = K Q^T into the columns the previous dQ^T used, once drained
-        if (!mbar_wait(bar_qf + st, (k >> 1) & 1, w)) break;
-        if (k > 0 && !mbar_wait(bar_dqfree, (k - 1) & 1, w)) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + 0, kK + koff(ks), kQ + st * kStageDesc + koff(ks), id_nn, ks > 0 ? 1u : 0u);
-        mma_commit(bar_s);
-        // dP^T = V dO^T: its columns were read before the previous dS^T was published
-        if (!mbar_wait(bar_of, k & 1, w)) break;
-        tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tmem + 128, kV + koff(ks), kDO + koff(ks), id_nn, ks > 0 ? 1u : 0u);
-        mma_commit(bar_dp);
+        const bool more = k + 1 < n_steps;
         // dV += P^T dO: P^T (bf16) in TMEM columns [0,32) (queries 0-63) and [64,96)
         if (!mbar_wait(bar_p, k & 1, w)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ts(tmem + 256, tmem + (ks >> 2) * 64 + (ks & 3) * 8, mDO + moff(ks), id_acc,
-                 (acc0 | (ks > 0)) ? 1u : 0u);
-        mma_commit(bar_oe);
-        // dK += dS^T Q, then dQ^T = K^T dS^T over the 128 keys
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          at[ks] = tmem + (ks >> 2) * 64 + (ks & 3) * 8;
+          b[ks] = mDO + st * kStageDesc + moff(ks);
+        }
+        mma_ts_x8(tmem + 256, at, b, id_acc, acc0);
+        mma_commit(bar_oe + st);
+        // S^T of the next step over the score columns (P^T is consumed in order by dV)
+        if (more) {
+          if (!mbar_wait(bar_qf + (st ^ 1), ((k + 1) >> 1) & 1, w)) break;
+          tc_fence_after();
+          issue_s(k + 1);
+        }
+        // dK += dS^T Q (dS^T bf16 in TMEM columns [128,160) and [192,224)), then
+        // dQ^T = K^T dS^T over [128,256) (dS^T MN-major from shared memory)
         if (!mbar_wait(bar_ds, k & 1, w)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ss(tmem + 384, kDS + koff(ks), mQ + st * kStageDesc + moff(ks), id_acc, (acc0 | (ks > 0)) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          at[ks] = tmem + 128 + (ks >> 2) * 64 + (ks & 3) * 8;
+          b[ks] = mQ + st * kStageDesc + moff(ks);
+        }
+        mma_ts_x8(tmem + 384, at, b, id_acc, acc0);
         mma_commit(bar_qe + st);
-#pragma unroll 1
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ss(tmem + 0, mK + moff(ks), mDS + moff(ks), id_dq, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          a[ks] = mK + moff(ks);
+          b[ks] = mDS + moff(ks);
+        }
+        mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
         mma_commit(bar_dq);
+        // dP^T of the next step once dQ^T has left tensor memory
+        if (more) {
+          if (!mbar_wait(bar_dqfree, k & 1, w) || !mbar_wait(bar_of + (st ^ 1), ((k + 1) >> 1) & 1, w)) break;
+          tc_fence_after();
+          issue_dp(k + 1);
+        }
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(bar_done);

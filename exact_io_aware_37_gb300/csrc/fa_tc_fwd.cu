@@ -17,8 +17,8 @@
 //              running maximum grows by more than 2^8 (a lazy rescale: the
 //              final u / l uses the same reference maximum, so it is exact),
 //              and run the epilogue.
-//   The softmax warpgroups raise their register limit to 224 and the third
-//   warpgroup lowers its to 56 (setmaxnreg) so the 128 scores of a row stay
+//   The softmax warpgroups raise their register limit to 200 and the third
+//   warpgroup lowers its to 104 (setmaxnreg) so the 128 scores of a row stay
 //   in registers.
 //   warp 8     TMA producer: Q tiles once, then K_j / V_j into a ring of
 //              shared-memory stages (mbarrier full/empty pairs).
@@ -302,23 +302,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kVOff), C::kHalfBytes, 1024);
-      // S_t = Q_t K^T (both K-major): D/16 MMAs of K = 16
+      // S_t = Q_t K^T (both K-major): D/16 MMAs of K = 16, issued back to back
       auto issue_s = [&](int t, int s) {
-        const uint64_t a = dq0 + ((t * C::kTileBytes) >> 4);
-        const uint64_t bk = dk0 + ((s * C::kTileBytes) >> 4);
-#pragma unroll 1
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + t * 128, a + off, bk + off, id_s, ks > 0 ? 1u : 0u);
+        const uint64_t a0 = dq0 + ((t * C::kTileBytes) >> 4);
+        const uint64_t b0 = dk0 + ((s * C::kTileBytes) >> 4);
+        if constexpr (D == 128) {
+          uint64_t a[8], b[8];
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = ((ks >> 2) * C::kHalfBytes + (ks & 3) * 32) >> 4;
+            a[ks] = a0 + off;
+            b[ks] = b0 + off;
+          }
+          mma_ss_x8(tmem + t * 128, a, b, id_s, 0u);
+        } else {
+          uint64_t a[4], b[4];
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            a[ks] = a0 + ks * 2;
+            b[ks] = b0 + ks * 2;
+          }
+          mma_ss_x4(tmem + t * 128, a, b, id_s, 0u);
         }
       };
       // O_t += P_t V (P from TMEM, V MN-major): 8 MMAs of K = 16 keys
       auto issue_pv = [&](int t, int s, bool acc) {
-        const uint64_t bv = dv0 + ((s * C::kTileBytes) >> 4);
-#pragma unroll 1
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bv + ((ks * 2048) >> 4), id_o,
-                 (acc || ks > 0) ? 1u : 0u);
+        const uint64_t b0 = dv0 + ((s * C::kTileBytes) >> 4);
+        uint32_t a[8];
+        uint64_t b[8];
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          a[ks] = tmem + t * 128 + ks * 8;
+          b[ks] = b0 + ((ks * 2048) >> 4);
+        }
+        mma_ts_x8(tmem + 256 + t * 128, a, b, id_o, acc ? 1u : 0u);
       };
       bool ok = mbar_wait(&bar_q, 0, w) && mbar_wait(&bar_k[0], 0, w);
       if (ok) {

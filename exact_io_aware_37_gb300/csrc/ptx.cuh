@@ -107,8 +107,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 // launch budget or the raise would wait forever: the static_assert checks the
 // arithmetic and build.py checks that ptxas gave the kernels kLaunchRegs.
 constexpr int kLaunchRegs = 168;
-constexpr int kComputeRegs = 224;
-constexpr int kSupportRegs = 56;
+constexpr int kComputeRegs = 200;
+constexpr int kSupportRegs = 104;
 static_assert(2 * 128 * kComputeRegs + 128 * kSupportRegs <= 384 * kLaunchRegs,
               "register split exceeds the launch budget");
 
@@ -280,6 +280,56 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Back-to-back groups of MMAs issued from one asm block, so no other
+// instruction of the issuing thread sits between them (each tcgen05.mma
+// occupies the issuer until the previous one has nearly finished, so any
+// instruction in between adds directly to the per-MMA time).  The first MMA
+// accumulates iff `acc` != 0; the others always accumulate.
+__device__ __forceinline__ void mma_ss_x4(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %9, 0;\n setp.eq.b32 q, %9, %9;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, q;\n}\n" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc), "r"(idesc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_x8(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %17, 0;\n setp.eq.b32 q, %17, %17;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %18, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %18, q;\n}\n" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]),
+      "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc), "r"(idesc)
+      : "memory");
+}
+// Same with A read from tensor memory at column addresses a[i].
+__device__ __forceinline__ void mma_ts_x8(uint32_t d, const uint32_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %17, 0;\n setp.eq.b32 q, %17, %17;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %18, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %18, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %18, q;\n}\n" ::"r"(d),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]),
+      "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc), "r"(idesc)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
