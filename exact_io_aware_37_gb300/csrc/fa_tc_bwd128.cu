@@ -22,8 +22,11 @@
 //
 // Warp roles (16 warps): 0-3 and 4-7 compute P^T and dS^T for query columns
 // [0,64) and [64,128); 8 = TMA / L / D producer; 9 = MMA issuer; 10-11 idle;
-// 12-15 drain dQ^T from tensor memory into the float32 accumulator with
-// reductions whose 32 lanes cover one contiguous 128-byte line.
+// 12-15 drain dQ^T: they copy it from tensor memory into shared memory (the
+// dS^T buffer, free once dQ^T has been formed, holds queries 0-63; a staging
+// buffer holds 64-127) and let the copy engine add each half into the
+// float32 accumulator (cp.reduce.async.bulk), so the next step's dP^T waits
+// only for the tensor-memory read-out.
 // Registers: 128 per thread at launch, then 176 for the two compute
 // warpgroups, 104 for the producer / MMA warpgroup and 56 for the drain
 // warpgroup (setmaxnreg).
@@ -72,11 +75,12 @@ constexpr int kTileBytes = kTile * D * 2;  // 32 KB
 constexpr int kHalfBytes = kTile * 128;    // 16 KB: 64 columns of 128 rows
 constexpr int kKOff = 0;
 constexpr int kVOff = kTileBytes;
-constexpr int kQOff = 2 * kTileBytes;      // 2 stages
-constexpr int kDOOff = 4 * kTileBytes;     // 2 stages
-constexpr int kDSOff = 6 * kTileBytes;     // dS^T [128 keys][128 queries] bf16
-constexpr int kLOff = kDSOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
-constexpr int kDvOff = kLOff + 1024;        // 2 x 128 floats: D
+constexpr int kQOff = 2 * kTileBytes;       // 2 stages
+constexpr int kDOOff = 4 * kTileBytes;      // 1 stage
+constexpr int kDSOff = 5 * kTileBytes;      // dS^T [128 keys][128 queries] bf16; dQ staging for queries 0-63
+constexpr int kStageOff = 6 * kTileBytes;   // dQ staging for queries 64-127: [64 queries][128] fp32
+constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
+constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
 constexpr int kBarOff = kDvOff + 1024;
 constexpr int kNumBars = 16;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -94,15 +98,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_kv = bars + 0;      // K, V loaded
   uint64_t* bar_qf = bars + 1;      // [2] Q tile + L / D of a stage loaded
   uint64_t* bar_qe = bars + 3;      // [2] Q / L / D stage free (dK done)
-  uint64_t* bar_of = bars + 5;      // [2] dO tile loaded
-  uint64_t* bar_oe = bars + 7;      // [2] dO stage free (dV done)
-  uint64_t* bar_s = bars + 9;       // S^T ready
-  uint64_t* bar_dp = bars + 10;     // dP^T ready
-  uint64_t* bar_p = bars + 11;      // P^T written (8 compute warps)
-  uint64_t* bar_ds = bars + 12;     // dS^T written (8 compute warps)
-  uint64_t* bar_dq = bars + 13;     // dQ^T ready
-  uint64_t* bar_dqfree = bars + 14; // dQ^T read out of TMEM (4 drain warps)
-  uint64_t* bar_done = bars + 15;   // every MMA complete
+  uint64_t* bar_of = bars + 5;      // dO tile loaded
+  uint64_t* bar_oe = bars + 6;      // dO buffer free (dV done)
+  uint64_t* bar_s = bars + 7;       // S^T ready
+  uint64_t* bar_dp = bars + 8;      // dP^T ready
+  uint64_t* bar_p = bars + 9;       // P^T written (8 compute warps)
+  uint64_t* bar_ds = bars + 10;     // dS^T written (8 compute warps)
+  uint64_t* bar_dq = bars + 11;     // dQ^T ready
+  uint64_t* bar_dqfree = bars + 12; // dQ^T read out of TMEM (4 drain warps)
+  uint64_t* bar_dsfree = bars + 13; // dS^T shared buffer no longer read by the copy engine
+  uint64_t* bar_done = bars + 14;   // every MMA complete
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
   float* s_l = reinterpret_cast<float*>(smem + kLOff);
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint64_t* bar = bars + i;
-      mbar_init(bar, (bar == bar_p || bar == bar_ds) ? 8 : (bar == bar_dqfree ? 4 : 1));
+      mbar_init(bar, (bar == bar_p || bar == bar_ds) ? 8 : (bar == bar_dqfree ? 4 : 1));  // bar_dsfree: the drain leader
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -217,6 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       tmem_ld32(t_dp + 32, sv[1]);
       tmem_ld_wait(sv[0]);
       tmem_ld_wait(sv[1]);
+      // the shared dS^T buffer doubled as dQ staging for the previous step
+      if (k > 0 && !warp_wait(bar_dsfree, (k - 1) & 1, w)) {
+        ok = false;
+        break;
+      }
       uint32_t dsp[32];
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
@@ -279,27 +289,49 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     const int quad = warp & 3;
     const int d = quad * 32 + lane;  // TMEM lane = head-width column of dQ^T
     const uint32_t t_dq = tmem + ((uint32_t)(quad * 32) << 16) + 128;
+    const bool leader = warp == kDrainWarp0 && lane == 0;
     for (int k = 0; k < n_steps; ++k) {
       const int q0 = (q_first + k) * kTile;
-      if (!warp_wait(bar_dq, k & 1, w)) break;
+      // the four drain warps decide together (they meet at named barriers below)
+      if (!named_bar_and(1, 128, warp_wait(bar_dq, k & 1, w))) break;
       tc_fence_after();
-      float* dst = p.dq_acc + (out_base + q0) * D + d;
 #pragma unroll 1
-      for (int c = 0; c < kTile / 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
+        // queries [32c, 32c+32): halves 0-63 go to the dS^T buffer, 64-127 to the staging buffer
+        float* buf = reinterpret_cast<float*>(smem + (c < 2 ? kDSOff : kStageOff)) + (c & 1) * 32 * D;
+        if (c == 2 && k > 0) {
+          // the staging buffer's previous reduction (the step before's second half) must have been read
+          if (leader) bulk_wait_read<1>();
+          named_bar_sync(1, 128);
+        }
         uint32_t v[32];
         tmem_ld32(t_dq + c * 32, v);
         tmem_ld_wait(v);
-        if (c == kTile / 32 - 1) {
+        if (c == 3) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_dqfree);  // the whole tile is out of tensor memory
         }
-        const int nq = min(32, len - (q0 + c * 32));
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (e < nq) atomicAdd(dst + (c * 32 + e) * D, __uint_as_float(v[e]));
+        for (int e = 0; e < 32; ++e) buf[e * D + d] = __uint_as_float(v[e]);
+        if (c & 1) {
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {
+            const int qh = q0 + (c >> 1) * 64;
+            const int nq = min(64, len - qh);
+            if (nq > 0) bulk_reduce_add_f32(p.dq_acc + (out_base + qh) * D, buf - 32 * D, (uint32_t)nq * D * 4);
+            bulk_commit();
+          }
+        }
+      }
+      // the first half lives in the dS^T buffer, which the next step rewrites
+      if (leader) {
+        bulk_wait_read<1>();
+        mbar_arrive(bar_dsfree);
       }
     }
+    if (leader) bulk_wait_all();
   } else {
     setmaxnreg_dec<kSupportRegs4>();
     if (warp == kTmaWarp) {
@@ -319,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       for (int k = 0; k < n_steps; ++k) {
         const int qi = q_first + k;
         const int st = k & 1;
-        // stage st was last used by step k - 2: its Q / L / D are free once that
-        // step's dK has completed, its dO once that step's dV has.
+        // Q / L / D stage st was last used by step k - 2 (free once its dK has
+        // completed); the single dO buffer by step k - 1 (free once its dV has).
         // Lane 0 waits and the answer is broadcast, so the warp never splits.
         int good = 1;
         if (lane == 0 && k >= 2) good = mbar_wait(bar_qe + st, ((k >> 1) - 1) & 1, w);
@@ -340,23 +372,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
             tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
                         row0 + qi * kTile, slab);
         }
-        if (lane == 0 && k >= 2) good = mbar_wait(bar_oe + st, ((k >> 1) - 1) & 1, w);
+        if (lane == 0 && k >= 1) good = mbar_wait(bar_oe, (k - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_of + st, kTileBytes);
+          mbar_arrive_expect_tx(bar_of, kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(smem + kDOOff + st * kTileBytes + hf * kHalfBytes, &p.tdo, bar_of + st, hf * 64,
-                        row0 + qi * kTile, slab);
+            tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, row0 + qi * kTile, slab);
         }
         issued = k + 1;
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
         mbar_wait_drain(bar_kv, 0, p.limit_ns);
-        for (int k = max(0, issued - 2); k < issued; ++k) {
+        if (issued > 0) mbar_wait_drain(bar_of, (issued - 1) & 1, p.limit_ns);
+        for (int k = max(0, issued - 2); k < issued; ++k)
           mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
-          mbar_wait_drain(bar_of + (k & 1), (k >> 1) & 1, p.limit_ns);
-        }
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -394,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           a[ks] = kV + koff(ks);
-          b[ks] = kDO + st * kStageDesc + koff(ks);
+          b[ks] = kDO + koff(ks);
         }
         mma_ss_x8(tmem + 128, a, b, id_nn, 0u);
         mma_commit(bar_dp);
@@ -417,10 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           at[ks] = tmem + (ks >> 2) * 64 + (ks & 3) * 8;
-          b[ks] = mDO + st * kStageDesc + moff(ks);
+          b[ks] = mDO + moff(ks);
         }
         mma_ts_x8(tmem + 256, at, b, id_acc, acc0);
-        mma_commit(bar_oe + st);
+        mma_commit(bar_oe);
         // S^T of the next step over the score columns (P^T is consumed in order by dV)
         if (more) {
           if (!mbar_wait(bar_qf + (st ^ 1), ((k + 1) >> 1) & 1, w)) break;
@@ -447,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         mma_commit(bar_dq);
         // dP^T of the next step once dQ^T has left tensor memory
         if (more) {
-          if (!mbar_wait(bar_dqfree, k & 1, w) || !mbar_wait(bar_of + (st ^ 1), ((k + 1) >> 1) & 1, w)) break;
+          if (!mbar_wait(bar_dqfree, k & 1, w) || !mbar_wait(bar_of, (k + 1) & 1, w)) break;
           tc_fence_after();
           issue_dp(k + 1);
         }
