@@ -177,19 +177,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
         const int k0 = j * kBN;
-        const bool mask = (p.causal && j == qt) || (k0 + kBN > len);
-        const int kmax = min(len, p.causal ? i + 1 : len) - k0;  // keys [k0, k0 + kmax) allowed
+        if ((p.causal && j == qt) || (k0 + kBN > len)) {
+          // diagonal or ragged tile: keys [k0, k0 + kmax) are allowed, the rest get -inf
+          const int kmax = min(len, p.causal ? i + 1 : len) - k0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= kmax) sr[c][e] = __float_as_uint(-INFINITY);
+        }
+        // row maximum of the raw scores (scale > 0 preserves the order)
         float mt = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(sr[c][e]) * p.c2;
-            if (mask && c * 32 + e >= kmax) x = -INFINITY;
-            sr[c][e] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
-          }
-        const float m_new = fmaxf(m_ref, mt);
+          for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+        const float m_new = fmaxf(m_ref, mt * p.c2);
         float alpha = 1.f;
         const bool grow = m_new > m_ref + kRescaleThreshold;
         if (grow) {
@@ -197,22 +200,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           m_ref = m_new;
           l *= alpha;
         }
-        const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
+        const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        // p = 2^(s * scale * log2(e) - m_ref), two columns per packed FMA
+        float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int e0 = 64 * hf + 2 * c;
-            const float p0 = ex2_approx(__uint_as_float(sr[e0 >> 5][e0 & 31]) - mu);
-            const float p1 = ex2_approx(__uint_as_float(sr[(e0 + 1) >> 5][(e0 + 1) & 31]) - mu);
-            rs += p0 + p1;
+            float a0, a1;
+            ffma2(a0, a1, __uint_as_float(sr[e0 >> 5][e0 & 31]), __uint_as_float(sr[(e0 + 1) >> 5][(e0 + 1) & 31]),
+                  p.c2, nmu, nmu);
+            const float p0 = ex2_approx(a0);
+            const float p1 = ex2_approx(a1);
+            fadd2(rs0, rs1, p0, p1);
             pk[c] = pack_bf16x2(p0, p1);
           }
           tmem_st32(t_s + 32 * hf, pk);
         }
-        l += rs;
+        l += rs0 + rs1;
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
           // accumulator rows rescaled in place: the previous PV is complete (the
           // wait on bar_s covers it) and this tile's PV waits for bar_p below
