@@ -189,9 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         const float4 l4 = sl4[c4];
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {
           const int c = 4 * c4 + e;
-          pr[c] = ex2_approx(fmaf(__uint_as_float(sv[c >> 5][c & 31]), p.c2, -lv[e]));
+          float a0, a1;  // s * scale * log2(e) - L * log2(e), two columns per packed FMA
+          ffma2(a0, a1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]), p.c2,
+                -lv[e], -lv[e + 1]);
+          pr[c] = ex2_approx(a0);
+          pr[c + 1] = ex2_approx(a1);
         }
       }
       if ((p.causal && qi == kt) || (kt * kTile + kTile > len) || (qi * kTile + kTile > len)) {
@@ -236,8 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c8 * 8 + 2 * e;
-          const float d0 = pr[c] * (__uint_as_float(sv[c >> 5][c & 31]) - dv[2 * e]);
-          const float d1 = pr[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - dv[2 * e + 1]);
+          float t0, t1, d0, d1;  // dS = P o (dP - D), two columns per packed op
+          fsub2(t0, t1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
+                dv[2 * e], dv[2 * e + 1]);
+          fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
           u[e] = pack_bf16x2(d0, d1);
         }
         // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
