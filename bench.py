@@ -41,8 +41,8 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 # kernel from one ncu capture, keyed by the SHA-256 of that kernel's source
 # file at capture time (reported as null once the source has changed).
 TRAFFIC_BY_SOURCE = {
-    # tc_bwd_kernel<128>, B2 H32 N4096 D128 causal: 405.3 MB read + 220.7 MB written
-    "4052612445c15265cc756e9587f07a76a47a181547882a4ba82151d961f759fc": 626.0e6,
+    # tc_bwd128_kernel, B2 H32 N4096 D128 causal: 405.1 MB read + 219.6 MB written
+    "dbd18fb3b2cfae03fbab64d79d21061493b7c64c8b34c65b2e2ca91d8ed76552": 624.7e6,
 }
 
 
@@ -61,7 +61,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+    """nvidia-smi samples (every 50 ms) taken while the timed region runs."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -76,7 +76,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, ValueError):
@@ -210,7 +210,7 @@ def run_reference(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -249,7 +249,11 @@ def main():
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_error() == 0
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in ev:  # create the events the library records around the main backward kernel
+        e[3].record(stream)
+        e[4].record(stream)
+    torch.cuda.synchronize()
     launches0 = fa.fa_launch_count()
     with ClockSampler(local) as clocks:
         barrier(dist)
@@ -261,6 +265,7 @@ def main():
             ev[s][0].record(stream)
             fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
             ev[s][1].record(stream)
+            fa.fa_bwd_time_main_kernel(ev[s][3], ev[s][4])
             fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
             ev[s][2].record(stream)
         t_end.record(stream)
@@ -271,6 +276,7 @@ def main():
     total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), device)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    main_ms = [e[3].elapsed_time(e[4]) for e in ev]  # main backward kernel alone
 
     f_fwd = flops_fwd(B, H, N, D, CAUSAL)
     f_step = 3.5 * f_fwd
@@ -281,11 +287,12 @@ def main():
     peak_tf, _, peak_kind = peaks()
     path = fa.fa_path_name(torch.bfloat16, D)
 
-    # dominant kernel: the backward pass (2.5x the forward FLOPs)
-    dom_ms = statistics.mean(bwd_ms)
-    dom_name = "fa_bwd (preprocess + main kernels)"
+    # dominant kernel: the main backward kernel (2.5x the forward FLOPs), timed
+    # by events the library records right around it
+    dom_ms = statistics.mean(main_ms)
+    dom_name = "tc_bwd128_kernel" if path == "tcgen05" else "simt backward kernels"
     src = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc",
-                       "fa_tc_bwd.cu" if path == "tcgen05" else "fa_simt.cu")
+                       "fa_tc_bwd128.cu" if path == "tcgen05" else "fa_simt.cu")
     traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src))
     achieved = 2.5 * f_fwd / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
@@ -302,7 +309,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         "fwd_frac_of_peak": fwd_tflops / peak_tf, "fwdbwd_frac_of_peak": value / world / peak_tf,
-        "ms_fwd": statistics.mean(fwd_ms), "ms_bwd": statistics.mean(bwd_ms),
+        "ms_fwd": statistics.mean(fwd_ms), "ms_bwd": statistics.mean(bwd_ms), "ms_bwd_main_kernel": dom_ms,
         "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clocks.summary(),

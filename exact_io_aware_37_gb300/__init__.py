@@ -18,7 +18,7 @@ import torch
 from ._lib import FA_BF16, FA_F32, FAError, lib, library_path  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
-           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "forward", "backward",
+           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
            "FAError"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
@@ -73,6 +73,12 @@ def fa_path_name(dtype, D):
 
 def fa_launch_count():
     return int(lib().fa_launch_count())
+
+
+def fa_bwd_time_main_kernel(start_event, stop_event):
+    """Have the next fa_bwd on this thread record the two torch.cuda.Events
+    (already recorded once, so they exist) around its main gradient kernel."""
+    lib().fa_bwd_time_main_kernel(start_event.cuda_event, stop_event.cuda_event)
 
 
 def fa_set_wait_limit_ns(limit_ns):

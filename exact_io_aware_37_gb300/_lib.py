@@ -30,6 +30,7 @@ SIGNATURES = {
     "fa_path_name": (_c.c_char_p, [_int, _int]),
     "fa_launch_count": (_c.c_ulonglong, []),
     "fa_last_error_detail": (_c.c_char_p, []),
+    "fa_bwd_time_main_kernel": (None, [_vp, _vp]),
 }
 
 

@@ -80,6 +80,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 void note_launches(unsigned n) { g_launches.fetch_add(n); }
 
 thread_local char g_detail[256];
+thread_local cudaEvent_t g_main_start = nullptr, g_main_stop = nullptr;
 
 cudaError_t note_error(const char* step, cudaError_t e) {
   if (e != cudaSuccess) snprintf(g_detail, sizeof(g_detail), "%s: %s", step, cudaGetErrorString(e));
@@ -138,6 +139,11 @@ const char* fa_path_name(fa_dtype dt, int D) {
 unsigned long long fa_launch_count(void) { return g_launches.load(); }
 
 const char* fa_last_error_detail(void) { return g_detail; }
+
+void fa_bwd_time_main_kernel(void* start_event, void* stop_event) {
+  g_main_start = static_cast<cudaEvent_t>(start_event);
+  g_main_stop = static_cast<cudaEvent_t>(stop_event);
+}
 
 void fa_set_wait_limit_ns(unsigned long long limit_ns) {
   g_wait_limit_ns.store(limit_ns < 1000ull ? 1000ull : limit_ns);
@@ -222,10 +228,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)rows * 4, 256))
                  : nullptr;
   g_detail[0] = 0;
+  cudaEvent_t ev_start = g_main_start, ev_stop = g_main_stop;
+  g_main_start = g_main_stop = nullptr;
   if (note_error("status word", status_word(&p.status)) != cudaSuccess) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool tc = kHaveTcBwd && use_tensor_cores(dt, D);
   cudaError_t e = launch_bwd_preprocess(p, dt, p.dq_acc != nullptr, s);
-  if (e == cudaSuccess) e = (kHaveTcBwd && use_tensor_cores(dt, D)) ? launch_tc_bwd(p, s) : launch_simt_bwd(p, dt, s);
+  if (e == cudaSuccess && ev_start) e = note_error("timing event", cudaEventRecord(ev_start, s));
+  if (e == cudaSuccess) e = tc ? launch_tc_bwd(p, s) : launch_simt_bwd(p, dt, s);
+  if (e == cudaSuccess && ev_stop) e = note_error("timing event", cudaEventRecord(ev_stop, s));
+  if (e == cudaSuccess && tc) e = launch_dq_convert(p, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

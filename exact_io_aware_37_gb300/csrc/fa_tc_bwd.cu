@@ -525,9 +525,7 @@ cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   dim3 grid((p.N + kBN - 1) / kBN, p.H, p.B);
   tc_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
   note_launches(1);
-  e = note_error("backward launch", cudaGetLastError());
-  if (e != cudaSuccess) return e;
-  return launch_dq_convert(p, s);
+  return note_error("backward launch", cudaGetLastError());
 }
 
 }  // namespace
@@ -546,10 +544,7 @@ cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s) {
 
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s) {
   if (p.D == 64) return launch_bwd_d<64>(p, s);
-  if (p.D == 128) {
-    const cudaError_t e = launch_tc_bwd128(p, s);
-    return e == cudaSuccess ? launch_dq_convert(p, s) : e;
-  }
+  if (p.D == 128) return launch_tc_bwd128(p, s);
   return cudaErrorInvalidValue;
 }
 

@@ -201,6 +201,15 @@ const char* fa_path_name(fa_dtype dtype, int D);
 const char* fa_last_error_detail(void);
 
 /*
+ * Instrumentation: the next fa_bwd call made on this host thread records
+ * `start_event` (a cudaEvent_t) on its stream right before its main
+ * gradient kernel and `stop_event` right after it, so a caller can time that
+ * kernel alone (the preprocess and dQ conversion launches fall outside).
+ * Either may be NULL.  The request is consumed by that call.
+ */
+void fa_bwd_time_main_kernel(void* start_event, void* stop_event);
+
+/*
  * Number of kernels this library has launched in this process (all devices,
  * all entry points, including failed launches it detected).  Host only.
  */
