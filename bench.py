@@ -331,45 +331,73 @@ def main():
 
 
 def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, args):
-    """Same metric through the public API with host buffers: every step copies
-    q, k, v, dO from pinned host memory, runs fa_fwd + fa_bwd and copies o,
-    lse, dq, dk, dv back, all inside the timed region."""
+    """Same metric through the public API with host buffers.  Every step copies
+    its q, k, v, dO from pinned host memory, runs fa_fwd + fa_bwd and copies o,
+    lse, dq, dk, dv back to pinned host memory, all inside the timed region.
+    Steps are pipelined the way a host-fed caller would run them: two sets of
+    device buffers, uploads on one stream, compute on another, downloads on a
+    third, so step i+1's upload and step i-1's download overlap step i."""
     hin = [x.pin_memory() for x in (q_h, k_h, v_h, do_h)]
-    dins = [torch.empty_like(x, device=device) for x in hin]
     B, H, N, D = q_h.shape
-    o = torch.empty_like(dins[0])
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
-    dq, dk, dv = (torch.empty_like(dins[0]) for _ in range(3))
-    ws = torch.empty(fa.fa_bwd_workspace_size(dins[0]), dtype=torch.uint8, device=device)
-    outs_d = [o, lse, dq, dk, dv]
-    outs_h = [torch.empty_like(x, device="cpu").pin_memory() for x in outs_d]
+    nbuf = 2
+    bufs = []
+    for _ in range(nbuf):
+        din = [torch.empty_like(x, device=device) for x in hin]
+        o = torch.empty_like(din[0])
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+        dq, dk, dv = (torch.empty_like(din[0]) for _ in range(3))
+        ws = torch.empty(fa.fa_bwd_workspace_size(din[0]), dtype=torch.uint8, device=device)
+        outs = [o, lse, dq, dk, dv]
+        hout = [torch.empty_like(x, device="cpu").pin_memory() for x in outs]
+        bufs.append((din, outs, ws, hout))
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev() for _ in range(nbuf)]
+    done = [ev() for _ in range(nbuf)]
+    out_done = [ev() for _ in range(nbuf)]
 
-    def step():
-        for hsrc, ddst in zip(hin, dins):
-            ddst.copy_(hsrc, non_blocking=True)
-        q, k, v, do = dins
-        fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
-        for dsrc, hdst in zip(outs_d, outs_h):
-            hdst.copy_(dsrc, non_blocking=True)
+    def run(steps, start_ev=None, end_ev=None):
+        if start_ev is not None:
+            start_ev.record(s_in)
+        for i in range(steps):
+            b = i % nbuf
+            din, outs, ws, hout = bufs[b]
+            if i >= nbuf:
+                s_in.wait_event(done[b])        # step i-2 has finished reading these inputs
+            with torch.cuda.stream(s_in):
+                for hsrc, ddst in zip(hin, din):
+                    ddst.copy_(hsrc, non_blocking=True)
+            in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            if i >= nbuf:
+                stream.wait_event(out_done[b])  # step i-2's results have been downloaded
+            q, k, v, do = din
+            o, lse, dq, dk, dv = outs
+            fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+            done[b].record(stream)
+            s_out.wait_event(done[b])
+            with torch.cuda.stream(s_out):
+                for dsrc, hdst in zip(outs, hout):
+                    hdst.copy_(dsrc, non_blocking=True)
+            out_done[b].record(s_out)
+        if end_ev is not None:
+            s_in.wait_stream(s_out)
+            end_ev.record(s_in)
 
-    for _ in range(3):
-        step()
+    run(4)
     torch.cuda.synchronize()
-    steps = max(3, args.steps // 2)
+    steps = max(4, args.steps // 4)
     barrier(dist)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    run(steps, a, b)
     torch.cuda.synchronize()
     ms = max_over_ranks(dist, a.elapsed_time(b), device) / steps
     f_step = 3.5 * flops_fwd(B, H, N, D, CAUSAL)
     return {"value": world * f_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in hin),
-            "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in outs_h),
-            "ms_per_step": ms}
+            "d2h_bytes_per_step": sum(x.numel() * x.element_size() for x in bufs[0][3]),
+            "ms_per_step": ms, "pipelined": "2 buffers; upload / compute / download streams"}
 
 
 if __name__ == "__main__":
