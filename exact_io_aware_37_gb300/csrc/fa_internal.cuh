@@ -63,6 +63,34 @@ __device__ __forceinline__ bool seq_range(const Problem& p, int b, int h, long l
   return true;
 }
 
+// Block order for causal grids shaped (items, H, B), where items differ in cost. The
+// flat block index is re-mapped so that the (b, h) pairs are cut into groups of about
+// `target_heads` (the group count is rounded up and the pairs spread evenly, so no group
+// is left nearly empty) and, inside a group, every head's rank-0 (heaviest) item is
+// handed out before any rank-1 item, and so on. The light items of one group then fill
+// in while the next group's heavy ones run, the grid ends on light items, and the
+// operands in use at any time belong to only a couple of groups of heads, which keeps
+// them in L2.
+struct GridItem {
+  int rank;  // 0 = heaviest
+  int b, h;
+};
+__device__ __forceinline__ GridItem grouped_heavy_first(int target_heads) {
+  const long long n_items = gridDim.x, n_bh = (long long)gridDim.y * gridDim.z;
+  const long long n_groups = (n_bh + target_heads - 1) / target_heads;
+  const long long per = (n_bh + n_groups - 1) / n_groups;  // heads in every group but the last
+  const long long flat = blockIdx.x + n_items * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+  const long long group = flat / (per * n_items);
+  const long long r = flat - group * per * n_items;
+  const long long heads = min(per, n_bh - group * per);
+  const long long bh = group * per + r % heads;
+  GridItem g;
+  g.rank = (int)(r / heads);
+  g.b = (int)(bh / gridDim.y);
+  g.h = (int)(bh % gridDim.y);
+  return g;
+}
+
 __device__ __forceinline__ float ld_elem(const float* p, long long i) { return p[i]; }
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
 __device__ __forceinline__ void st_elem(float* p, long long i, float x) { p[i] = x; }

@@ -50,6 +50,7 @@ constexpr int kThreads = 384;  // 2 softmax warpgroups + 1 support warpgroup
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr int kFwdHeadGroup = 16;  // heads per group of the causal block order (measured best of 8..64)
 
 struct FwdParams {
   CUtensorMap tq, tk, tv;
@@ -91,7 +92,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
+  // causal: pairs of late query tiles see the most keys and are handed out first
+  const GridItem item = p.causal ? grouped_heavy_first(kFwdHeadGroup) : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
+  const int b = item.b, h = item.h;
 
   // ---- the (sequence, head) this CTA works on
   int len, row0, slab;
@@ -114,8 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   }
   const int n_qt = (len + kBM - 1) / kBM;
   const int n_pairs = (n_qt + 1) / 2;
-  // causal: the last query tiles see the most keys, so they are scheduled first
-  const int pair = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int pair = p.causal ? (int)gridDim.x - 1 - item.rank : item.rank;
   if (pair >= n_pairs) return;
   const int qt0 = 2 * pair;
   const int n_kv = (len + kBN - 1) / kBN;

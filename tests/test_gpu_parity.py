@@ -31,6 +31,11 @@ DENSE_CASES = [
     (2, 2, 300, 64),
     (1, 1, 513, 128),
     (1, 2, 640, 64),
+    # many (b, h) pairs: the causal block order cuts them into several head groups,
+    # the last one short
+    (3, 6, 384, 128),
+    (5, 7, 300, 64),
+    (6, 3, 520, 128),
 ]
 
 
