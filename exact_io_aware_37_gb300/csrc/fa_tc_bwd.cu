@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           tma_load_3d(smem + C::kVOff + hf * C::kHalfBytes, &p.tv, bar_kv, hf * 64, row0 + kt * kBN, slab);
         }
       }
-      int issued = 0;
+      int q_issued = 0, o_issued = 0;
       for (int k = 0; k < n_steps; ++k) {
         const int qi = q_first + k;
         const int st = k & 1;
@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             tma_load_3d(smem + C::kQOff + st * C::kTileBytes + hf * C::kHalfBytes, &p.tq, bar_qf + st, hf * 64,
                         row0 + qi * kBM, slab);
         }
+        q_issued = k + 1;
         if (lane == 0 && k >= 2) good = mbar_wait(bar_oe + st, ((k >> 1) - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
@@ -371,15 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             tma_load_3d(smem + C::kDOOff + st * C::kTileBytes + hf * C::kHalfBytes, &p.tdo, bar_of + st,
                         hf * 64, row0 + qi * kBM, slab);
         }
-        issued = k + 1;
+        o_issued = k + 1;
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
         mbar_wait_drain(bar_kv, 0, p.limit_ns);
-        for (int k = max(0, issued - 2); k < issued; ++k) {
-          mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
-          mbar_wait_drain(bar_of + (k & 1), (k >> 1) & 1, p.limit_ns);
-        }
+        for (int k = max(0, q_issued - 2); k < q_issued; ++k) mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
+        for (int k = max(0, o_issued - 2); k < o_issued; ++k) mbar_wait_drain(bar_of + (k & 1), (k >> 1) & 1, p.limit_ns);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer

@@ -14,22 +14,26 @@
 //     [384,512) dK += dS^T Q        (A = dS^T from tensor memory)
 // dQ^T also needs dS^T as an MN-major shared-memory operand, so the compute
 // warps write it to both places.  The MMA order per step k is
-//     dV_k, S^T_{k+1}, dK_k, dQ^T_k, [dQ^T_k drained] dP^T_{k+1}
-// so the next step's P^T is built while dK, dQ and the drain of this step
-// run.  Shared-memory operand traffic is the limit of this formulation
-// (two SS products of 8 KB per 64-cycle MMA besides the TS ones), which is
-// why everything that can be read from tensor memory is.
+//     dP^T_k [after dQ^T_{k-1} is out], dV_k, S^T_{k+1}, dK_k, dQ^T_k
+// and the compute warps work through
+//     P^T_k, read out dQ^T_{k-1}, dS^T_k
+// so dP^T_k is formed while they copy dQ^T_{k-1} to shared memory, and the
+// next step's S^T while they build dS^T_k.
 //
-// Warp roles (16 warps): 0-3 and 4-7 compute P^T and dS^T for query columns
-// [0,64) and [64,128); 8 = TMA / L / D producer; 9 = MMA issuer; 10-11 idle;
-// 12-15 drain dQ^T: they copy it from tensor memory into shared memory (the
-// dS^T buffer, free once dQ^T has been formed, holds queries 0-63; a staging
-// buffer holds 64-127) and let the copy engine add each half into the
-// float32 accumulator (cp.reduce.async.bulk), so the next step's dP^T waits
-// only for the tensor-memory read-out.
-// Registers: 128 per thread at launch, then 176 for the two compute
-// warpgroups, 104 for the producer / MMA warpgroup and 56 for the drain
-// warpgroup (setmaxnreg).
+// Warp roles (12 warps): 0-3 and 4-7 compute P^T and dS^T for query columns
+// [0,64) and [64,128), and copy dQ^T for the same query columns out of
+// tensor memory into shared memory (half 0 into the dS^T buffer, which is
+// free between dQ^T_k and dS^T_{k+1}; half 1 into a buffer of its own);
+// 8 = TMA / L / D producer; 9 = MMA issuer; 10 = dQ reducer: it has the copy
+// engine add both halves into the float32 accumulator
+// (cp.reduce.async.bulk) and hands the buffers back once they have been
+// read; 11 idle.  A CTA can push only about 24 bytes per clock of
+// reductions out to L2, so the 64 KB of dQ per step are the backward's
+// other bound besides the tensor core; the compute warps therefore never
+// wait for a reduction except to reuse the dS^T buffer, and they form dS^T
+// in registers before that wait.
+// Registers: 168 per thread at launch, then 184 for the two compute
+// warpgroups and 136 for the producer / MMA warpgroup (setmaxnreg).
 #include <math.h>
 
 #include "fa_internal.cuh"
@@ -45,15 +49,15 @@ constexpr int D = 128;
 constexpr int kTile = 128;  // keys per CTA and queries per step
 constexpr int kBwdHeadGroup = 4;  // heads per group of the causal block order: Q, dO and the dQ
                                    // accumulator of a head take 4 MB at N = 4096 (measured best of 2..32)
-constexpr int kThreads = 512;
+constexpr int kThreads = 384;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kDrainWarp0 = 12;
-constexpr int kLaunchRegs4 = 128;
-constexpr int kComputeRegs4 = 176;
-constexpr int kSupportRegs4 = 104;  // producer / MMA warpgroup
-constexpr int kDrainRegs4 = 56;
-static_assert(2 * 128 * kComputeRegs4 + 128 * kSupportRegs4 + 128 * kDrainRegs4 <= kThreads * kLaunchRegs4,
+constexpr int kReduceWarp = 10;
+// setmaxnreg split of the kLaunchRegs budget: the MMA issuer keeps five groups of
+// eight descriptors in flight and needs more than the forward's support share
+constexpr int kBwdComputeRegs = 184;
+constexpr int kBwdSupportRegs = 136;
+static_assert(2 * 128 * kBwdComputeRegs + 128 * kBwdSupportRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
 
 struct Bwd128Params {
@@ -80,11 +84,11 @@ constexpr int kVOff = kTileBytes;
 constexpr int kQOff = 2 * kTileBytes;       // 2 stages
 constexpr int kDOOff = 4 * kTileBytes;      // 1 stage
 constexpr int kDSOff = 5 * kTileBytes;      // dS^T [128 keys][128 queries] bf16; dQ staging for queries 0-63
-constexpr int kStageOff = 6 * kTileBytes;   // dQ staging for queries 64-127: [64 queries][128] fp32
+constexpr int kStageOff = 6 * kTileBytes;   // dQ staging for queries 64-127: [64 queries][D] fp32
 constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
 constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
 constexpr int kBarOff = kDvOff + 1024;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 18;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* bar_kv = bars + 0;      // K, V loaded
-  uint64_t* bar_qf = bars + 1;      // [2] Q tile + L / D of a stage loaded
+  uint64_t* bar_qf = bars + 1;      // [2] Q tile + L / D of a stage loaded (2 arrivals + bytes)
   uint64_t* bar_qe = bars + 3;      // [2] Q / L / D stage free (dK done)
   uint64_t* bar_of = bars + 5;      // dO tile loaded
   uint64_t* bar_oe = bars + 6;      // dO buffer free (dV done)
@@ -107,9 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_p = bars + 9;       // P^T written (8 compute warps)
   uint64_t* bar_ds = bars + 10;     // dS^T written (8 compute warps)
   uint64_t* bar_dq = bars + 11;     // dQ^T ready
-  uint64_t* bar_dqfree = bars + 12; // dQ^T read out of TMEM (4 drain warps)
-  uint64_t* bar_dsfree = bars + 13; // dS^T shared buffer no longer read by the copy engine
+  uint64_t* bar_dqfree = bars + 12; // dQ^T read out of TMEM (8 compute warps)
+  uint64_t* bar_dsfree = bars + 13; // dS^T buffer no longer read by the copy engine (reducer)
   uint64_t* bar_done = bars + 14;   // every MMA complete
+  uint64_t* bar_staged = bars + 15; // [2] dQ half staged in shared memory (4 warps each)
+  uint64_t* bar_stfree = bars + 17; // half 1's staging buffer read by the copy engine (reducer)
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
   float* s_l = reinterpret_cast<float*>(smem + kLOff);
@@ -144,7 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint64_t* bar = bars + i;
-      mbar_init(bar, (bar == bar_p || bar == bar_ds) ? 8 : (bar == bar_dqfree ? 4 : 1));  // bar_dsfree: the drain leader
+      const bool by8 = bar == bar_p || bar == bar_ds || bar == bar_dqfree;
+      const bool by4 = bar == bar_staged || bar == bar_staged + 1;
+      const bool by2 = bar == bar_qf || bar == bar_qf + 1;  // Q bytes + L / D written
+      mbar_init(bar, by8 ? 8 : by4 ? 4 : by2 ? 2 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -160,26 +169,48 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   const WaitCtx w{abort_flag, p.status, p.limit_ns};
 
   if (warp < 8) {
-    // ------------------------------------------------------------ P^T, dS^T, epilogue
-    setmaxnreg_inc<kComputeRegs4>();
+    // ------------------------------------------------------------ P^T, dS^T, dQ^T read-out, epilogue
+    setmaxnreg_inc<kBwdComputeRegs>();
     const int ch = warp >> 2;        // query-column half
     const int quad = warp & 3;       // TMEM lanes 32*quad ..
-    const int j = quad * 32 + lane;  // key row within the tile
+    const int j = quad * 32 + lane;  // key row of S^T / dP^T; head-width column of dQ^T
     const int key = kt * kTile + j;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + ch * 64;
-    const uint32_t t_dp = tmem + lane_off + 128 + ch * 64;
+    const uint32_t t_dp = tmem + lane_off + 128 + ch * 64;  // dP^T, dS^T, then dQ^T of this half
     uint8_t* ds_row = smem + kDSOff + ch * kHalfBytes + (j >> 3) * 1024 + (j & 7) * 128;
-    bool ok = true;
+    float* stage = reinterpret_cast<float*>(smem + (ch == 0 ? kDSOff : kStageOff));
+    bool ok = true;  // once a wait fails the rest are skipped (the abort flag is set)
+
+    // dQ^T of step kk leaves tensor memory: this warp holds head-width column j
+    // for its half's 64 queries and writes them as rows [64 queries][D] fp32.
+    auto drain_dq = [&](int kk) {
+      ok = ok && warp_wait(bar_dq, kk & 1, w);
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld32(t_dp, v[0]);
+      tmem_ld32(t_dp + 32, v[1]);
+      tmem_ld_wait(v[0]);
+      tmem_ld_wait(v[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqfree);
+      // half 1's buffer must have been read by the previous reduction (half 0's
+      // buffer is the dS^T buffer, already released before dS^T_kk was written)
+      if (ch == 1 && kk > 0) ok = ok && warp_wait(bar_stfree, (kk - 1) & 1, w);
+#pragma unroll
+      for (int e = 0; e < 64; ++e) stage[e * D + j] = __uint_as_float(v[e >> 5][e & 31]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_staged + ch);
+    };
+
     for (int k = 0; k < n_steps; ++k) {
       const int qi = q_first + k;
       const int st = k & 1;
       const float4* sl4 = reinterpret_cast<const float4*>(s_l + st * 128 + ch * 64);
       const float4* sd4 = reinterpret_cast<const float4*>(s_d + st * 128 + ch * 64);
-      if (!warp_wait(bar_qf + st, (k >> 1) & 1, w) || !warp_wait(bar_s, k & 1, w)) {
-        ok = false;
-        break;
-      }
+      ok = ok && warp_wait(bar_qf + st, (k >> 1) & 1, w) && warp_wait(bar_s, k & 1, w);
       tc_fence_after();
       uint32_t sv[2][32];
       tmem_ld32(t_s, sv[0]);
@@ -221,26 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
 
-      if (!warp_wait(bar_dp, k & 1, w)) {
-        ok = false;
-        break;
-      }
+      if (k > 0) drain_dq(k - 1);
+
+      ok = ok && warp_wait(bar_dp, k & 1, w);
       tc_fence_after();
       tmem_ld32(t_dp, sv[0]);
       tmem_ld32(t_dp + 32, sv[1]);
       tmem_ld_wait(sv[0]);
       tmem_ld_wait(sv[1]);
-      // the shared dS^T buffer doubled as dQ staging for the previous step
-      if (k > 0 && !warp_wait(bar_dsfree, (k - 1) & 1, w)) {
-        ok = false;
-        break;
-      }
       uint32_t dsp[32];
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         const float4 da = sd4[2 * c8], db = sd4[2 * c8 + 1];
         const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-        uint32_t u[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c8 * 8 + 2 * e;
@@ -248,22 +272,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           fsub2(t0, t1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
                 dv[2 * e], dv[2 * e + 1]);
           fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
-          u[e] = pack_bf16x2(d0, d1);
+          dsp[4 * c8 + e] = pack_bf16x2(d0, d1);
         }
-        // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
-        *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
-        dsp[4 * c8 + 0] = u[0];
-        dsp[4 * c8 + 1] = u[1];
-        dsp[4 * c8 + 2] = u[2];
-        dsp[4 * c8 + 3] = u[3];
       }
       tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
+      // the dS^T buffer held half 0 of the previous dQ until the copy engine read it
+      if (k > 0) ok = ok && warp_wait(bar_dsfree, (k - 1) & 1, w);
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)  // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
+        *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) =
+            make_uint4(dsp[4 * c8], dsp[4 * c8 + 1], dsp[4 * c8 + 2], dsp[4 * c8 + 3]);
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
+    drain_dq(n_steps - 1);
     // epilogue: dV and dK rows of this CTA's keys
     if (ok && warp_wait(bar_done, 0, w)) {
       tc_fence_after();
@@ -293,57 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         }
       }
     }
-  } else if (warp >= kDrainWarp0) {
-    // ------------------------------------------------------------ dQ drain
-    setmaxnreg_dec<kDrainRegs4>();
-    const int quad = warp & 3;
-    const int d = quad * 32 + lane;  // TMEM lane = head-width column of dQ^T
-    const uint32_t t_dq = tmem + ((uint32_t)(quad * 32) << 16) + 128;
-    const bool leader = warp == kDrainWarp0 && lane == 0;
-    for (int k = 0; k < n_steps; ++k) {
-      const int q0 = (q_first + k) * kTile;
-      // the four drain warps decide together (they meet at named barriers below)
-      if (!named_bar_and(1, 128, warp_wait(bar_dq, k & 1, w))) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        // queries [32c, 32c+32): halves 0-63 go to the dS^T buffer, 64-127 to the staging buffer
-        float* buf = reinterpret_cast<float*>(smem + (c < 2 ? kDSOff : kStageOff)) + (c & 1) * 32 * D;
-        if (c == 2 && k > 0) {
-          // the staging buffer's previous reduction (the step before's second half) must have been read
-          if (leader) bulk_wait_read<1>();
-          named_bar_sync(1, 128);
-        }
-        uint32_t v[32];
-        tmem_ld32(t_dq + c * 32, v);
-        tmem_ld_wait(v);
-        if (c == 3) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_dqfree);  // the whole tile is out of tensor memory
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) buf[e * D + d] = __uint_as_float(v[e]);
-        if (c & 1) {
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (leader) {
-            const int qh = q0 + (c >> 1) * 64;
-            const int nq = min(64, len - qh);
-            if (nq > 0) bulk_reduce_add_f32(p.dq_acc + (out_base + qh) * D, buf - 32 * D, (uint32_t)nq * D * 4);
-            bulk_commit();
-          }
-        }
-      }
-      // the first half lives in the dS^T buffer, which the next step rewrites
-      if (leader) {
-        bulk_wait_read<1>();
-        mbar_arrive(bar_dsfree);
-      }
-    }
-    if (leader) bulk_wait_all();
   } else {
-    setmaxnreg_dec<kSupportRegs4>();
+    setmaxnreg_dec<kBwdSupportRegs>();
     if (warp == kTmaWarp) {
       // ---------------------------------------------------------- producer
       if (lane == 0) {
@@ -357,31 +333,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           tma_load_3d(smem + kVOff + hf * kHalfBytes, &p.tv, bar_kv, hf * 64, row0 + kt * kTile, slab);
         }
       }
-      int issued = 0;
+      int q_issued = 0, o_issued = 0;
       for (int k = 0; k < n_steps; ++k) {
         const int qi = q_first + k;
         const int st = k & 1;
         // Q / L / D stage st was last used by step k - 2 (free once its dK has
         // completed); the single dO buffer by step k - 1 (free once its dV has).
         // Lane 0 waits and the answer is broadcast, so the warp never splits.
+        // L and D of the tile are fetched before the wait, so the Q copy goes out
+        // as soon as its stage is free; the stage's barrier takes a second
+        // arrival once they are in shared memory.
+        float lv[4], dv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int qrow = qi * kTile + lane * 4 + e;
+          const bool in = qrow < len;
+          lv[e] = in ? p.lse[out_base + qrow] * kLog2e : 0.f;
+          dv[e] = in ? p.dvec[out_base + qrow] : 0.f;
+        }
         int good = 1;
         if (lane == 0 && k >= 2) good = mbar_wait(bar_qe + st, ((k >> 1) - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = lane * 4 + e;
-          const int qrow = qi * kTile + r;
-          const bool in = qrow < len;
-          s_l[st * 128 + r] = in ? p.lse[out_base + qrow] * kLog2e : 0.f;
-          s_d[st * 128 + r] = in ? p.dvec[out_base + qrow] : 0.f;
-        }
-        __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(bar_qf + st, kTileBytes);
           for (int hf = 0; hf < 2; ++hf)
             tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
                         row0 + qi * kTile, slab);
         }
+        q_issued = k + 1;
+        *reinterpret_cast<float4*>(s_l + st * 128 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+        *reinterpret_cast<float4*>(s_d + st * 128 + lane * 4) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_qf + st);
         if (lane == 0 && k >= 1) good = mbar_wait(bar_oe, (k - 1) & 1, w);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
@@ -389,15 +372,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           for (int hf = 0; hf < 2; ++hf)
             tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, row0 + qi * kTile, slab);
         }
-        issued = k + 1;
+        o_issued = k + 1;
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
         mbar_wait_drain(bar_kv, 0, p.limit_ns);
-        if (issued > 0) mbar_wait_drain(bar_of, (issued - 1) & 1, p.limit_ns);
-        for (int k = max(0, issued - 2); k < issued; ++k)
+        if (o_issued > 0) mbar_wait_drain(bar_of, (o_issued - 1) & 1, p.limit_ns);
+        for (int k = max(0, q_issued - 2); k < q_issued; ++k)
           mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
       }
+    } else if (warp == kReduceWarp && lane == 0) {
+      // ---------------------------------------------------------- dQ reducer
+      // Both halves go out back to back; half 0's buffer (the dS^T buffer) is
+      // handed back as soon as it has been read, half 1's after that.
+      for (int kk = 0; kk < n_steps; ++kk) {
+        const int q0 = (q_first + kk) * kTile;
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(bar_staged + hf, kk & 1, w)) break;
+          const int nq = min(64, len - (q0 + hf * 64));
+          if (nq > 0)
+            bulk_reduce_add_f32(p.dq_acc + (out_base + q0 + hf * 64) * D, smem + (hf == 0 ? kDSOff : kStageOff),
+                                (uint32_t)nq * D * 4);
+          bulk_commit();
+        }
+        if (*abort_flag) break;
+        bulk_wait_read<1>();  // half 0 read
+        mbar_arrive(bar_dsfree);
+        bulk_wait_read<0>();  // half 1 read
+        mbar_arrive(bar_stfree);
+      }
+      bulk_wait_all();
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t id_nn = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
@@ -429,8 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         mma_ss_x8(tmem + 0, a, b, id_nn, 0u);
         mma_commit(bar_s);
       };
-      auto issue_dp = [&](int k) {  // dP^T_k = V dO_k^T -> [128,256)
-        const int st = k & 1;
+      auto issue_dp = [&]() {  // dP^T_k = V dO_k^T -> [128,256)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           a[ks] = kV + koff(ks);
@@ -445,12 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         issue_s(0);
         ok = mbar_wait(bar_of, 0, w);
         tc_fence_after();
-        if (ok) issue_dp(0);
+        if (ok) issue_dp();
       }
       for (int k = 0; ok && k < n_steps; ++k) {
         const int st = k & 1;
         const uint32_t acc0 = k > 0 ? 1u : 0u;
         const bool more = k + 1 < n_steps;
+        // dP^T_k over [128,256) once dQ^T_{k-1} has left it (dP^T_0 went out with S^T_0)
+        if (k > 0) {
+          if (!mbar_wait(bar_dqfree, (k - 1) & 1, w) || !mbar_wait(bar_of, k & 1, w)) break;
+          tc_fence_after();
+          issue_dp();
+        }
         // dV += P^T dO: P^T (bf16) in TMEM columns [0,32) (queries 0-63) and [64,96)
         if (!mbar_wait(bar_p, k & 1, w)) break;
         tc_fence_after();
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           b[ks] = mDO + moff(ks);
         }
         mma_ts_x8(tmem + 256, at, b, id_acc, acc0);
-        mma_commit(bar_oe);
+        mma_commit(bar_oe);  // dP^T_k and dV_k were the dO tile's last readers
         // S^T of the next step over the score columns (P^T is consumed in order by dV)
         if (more) {
           if (!mbar_wait(bar_qf + (st ^ 1), ((k + 1) >> 1) & 1, w)) break;
@@ -485,12 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         }
         mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
         mma_commit(bar_dq);
-        // dP^T of the next step once dQ^T has left tensor memory
-        if (more) {
-          if (!mbar_wait(bar_dqfree, k & 1, w) || !mbar_wait(bar_of, (k + 1) & 1, w)) break;
-          tc_fence_after();
-          issue_dp(k + 1);
-        }
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(bar_done);
