@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ __align__(8) uint64_t bar_q, bar_done;
-  __shared__ __align__(8) uint64_t bar_k[C::kStages], bar_v[C::kStages], bar_free[C::kStages];
+  __shared__ __align__(8) uint64_t bar_k[C::kStages], bar_v[C::kStages], bar_free[C::kStages], bar_step0;
   __shared__ __align__(8) uint64_t bar_s[2], bar_p[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       mbar_init(&bar_v[s], 1);
       mbar_init(&bar_free[s], 1);
     }
+    mbar_init(&bar_step0, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], 4);  // one arrival per softmax warp
@@ -280,10 +281,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         for (int hf = 0; hf < C::kHalves; ++hf)
           tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
                       row0 + (qt0 + t) * kBM, slab);
+      // Each mbarrier operation of the MMA thread costs it ~150 clk (and the tensor
+      // pipe the same idle time), so with two stages it commits no per-step
+      // "stage free" barrier: loading
+      // K_j / V_j needs step j - 2 complete, which is completion j - 1 of the S
+      // barrier of the last query tile (completion 0 is the prologue's S_0; its
+      // commit after step i follows every MMA of that step).  A parity wait is
+      // only unambiguous if at least j - 1 and at most j completions can have
+      // happened: at most j holds because completion j needs S(j), i.e. K_j,
+      // which is not loaded yet; at least j - 1 holds from j = 3 on because the
+      // load of j - 1 waited for completion j - 2, and for j = 2 a one-off
+      // barrier committed after step 0 is used instead.
+      const int t_last = nkv[1] > 0 ? 1 : 0;
       int issued = 0;
       for (int j = 0; j < nmax; ++j) {
         const int s = j % C::kStages, round = j / C::kStages;
-        if (round > 0 && !mbar_wait(&bar_free[s], (round - 1) & 1, w)) break;
+        if (round > 0) {
+          bool freed;
+          if (C::kStages != 2)
+            freed = mbar_wait(&bar_free[s], (round - 1) & 1, w);
+          else if (j == 2)
+            freed = mbar_wait(&bar_step0, 0, w);
+          else
+            freed = mbar_wait(&bar_s[t_last], (j - 1) & 1, w);
+          if (!freed) break;
+        }
         mbar_arrive_expect_tx(&bar_k[s], C::kTileBytes);
         for (int hf = 0; hf < C::kHalves; ++hf)
           tma_load_3d(smem + C::kKOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_k[s], hf * 64,
@@ -381,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
           mma_commit(&bar_s[t]);
         }
-        if (ok) mma_commit(&bar_free[s]);
+        if (ok && C::kStages != 2) mma_commit(&bar_free[s]);
+        if (ok && C::kStages == 2 && j == 0) mma_commit(&bar_step0);
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(&bar_done);
