@@ -215,6 +215,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
+                    help="16-bit input type (the same synthetic draws, rounded to it)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -229,7 +231,7 @@ def main():
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    cfg = synth.WORKLOADS[WORKLOAD]
+    cfg = dict(synth.WORKLOADS[WORKLOAD], dtype=args.dtype)
     q_h, k_h, v_h, do_h = synth.make_dense(cfg)
     B, H, N, D = q_h.shape
     scale = 1.0 / D ** 0.5
@@ -285,7 +287,7 @@ def main():
     fwd_tflops = f_fwd / (statistics.mean(fwd_ms) * 1e-3) / 1e12
     bwd_tflops = 2.5 * f_fwd / (statistics.mean(bwd_ms) * 1e-3) / 1e12
     peak_tf, _, peak_kind = peaks()
-    path = fa.fa_path_name(torch.bfloat16, D)
+    path = fa.fa_path_name(q.dtype, D)
 
     # dominant kernel: the main backward kernel (2.5x the forward FLOPs), timed
     # by events the library records right around it
@@ -293,16 +295,18 @@ def main():
     dom_name = "tc_bwd128_kernel" if path == "tcgen05" else "simt backward kernels"
     src = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc",
                        "fa_tc_bwd128.cu" if path == "tcgen05" else "fa_simt.cu")
-    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src))
+    # the ncu capture behind the table was of the bf16 run
+    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src)) if args.dtype == "bf16" else None
     achieved = 2.5 * f_fwd / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": traffic, "kernel": dom_name,
-                "peak_kind": f"bf16 dense burst, {peak_kind}"}
+                "peak_kind": f"bf16 dense burst, {peak_kind}" + (
+                    "" if args.dtype == "bf16" else "; fp16 has the same nominal dense rate")}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.dtype == "bf16" else METRIC.replace("bf16", args.dtype), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} causal", "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
                    "kernel_path": path,
                    "l2": f"inputs {4 * q.numel() * 2 / 2**20:.0f} MiB > 129 MiB L2; no flush",

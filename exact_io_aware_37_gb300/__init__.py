@@ -15,13 +15,13 @@ import math
 
 import torch
 
-from ._lib import FA_BF16, FA_F32, FAError, lib, library_path  # noqa: F401
+from ._lib import FA_BF16, FA_F16, FA_F32, FAError, lib, library_path  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
            "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
            "FAError"]
 
-_DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32}
+_DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.float16: FA_F16}
 
 
 def _ptr(t):

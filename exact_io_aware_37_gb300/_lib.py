@@ -5,7 +5,7 @@ import os
 
 from . import build as _build
 
-FA_BF16, FA_F32 = 0, 1
+FA_BF16, FA_F32, FA_F16 = 0, 1, 2
 STATUS = {
     0: "FA_OK", -1: "FA_ERR_INVALID", -2: "FA_ERR_UNSUPPORTED", -3: "FA_ERR_ALIGN",
     -4: "FA_ERR_CUDA", -5: "FA_ERR_TIMEOUT", -6: "FA_ERR_WORKSPACE",

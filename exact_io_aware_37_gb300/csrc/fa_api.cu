@@ -43,17 +43,17 @@ cudaError_t status_word(unsigned** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The tensor-core kernels cover bf16 with D in {64, 128}.
+// The tensor-core kernels cover bf16 and fp16 with D in {64, 128}.
 constexpr bool kHaveTcFwd = true;
 constexpr bool kHaveTcBwd = true;
-bool use_tensor_cores(fa_dtype dt, int D) { return dt == FA_BF16 && (D == 64 || D == 128); }
+bool use_tensor_cores(fa_dtype dt, int D) { return (dt == FA_BF16 || dt == FA_F16) && (D == 64 || D == 128); }
 
 fa_status validate(int B, int H, int N, int D, float scale, int causal, const int32_t* cu, int T, fa_dtype dt) {
   if (B < 0 || H < 0 || N < 0 || D <= 0) return FA_ERR_INVALID;
   if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;  // grid y / z limits
   if (!isfinite(scale)) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
-  if (dt != FA_BF16 && dt != FA_F32) return FA_ERR_UNSUPPORTED;
+  if (dt != FA_BF16 && dt != FA_F32 && dt != FA_F16) return FA_ERR_UNSUPPORTED;
   if (fa_path_name(dt, D) == nullptr) return FA_ERR_UNSUPPORTED;
   if (cu != nullptr && T < 0) return FA_ERR_INVALID;
   return FA_OK;
@@ -130,8 +130,8 @@ const char* fa_strerror(fa_status s) {
 }
 
 const char* fa_path_name(fa_dtype dt, int D) {
-  if (dt == FA_BF16 && (D == 64 || D == 128))
-    return kHaveTcFwd ? (kHaveTcBwd ? "tcgen05" : "tcgen05_fwd+simt_bwd") : "simt_bf16";
+  if ((dt == FA_BF16 || dt == FA_F16) && (D == 64 || D == 128))
+    return kHaveTcFwd ? (kHaveTcBwd ? "tcgen05" : "tcgen05_fwd+simt_bwd") : "simt_16bit";
   if (dt == FA_F32 && (D == 32 || D == 64 || D == 128)) return "simt_f32";
   return nullptr;
 }
@@ -193,6 +193,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   Problem p{};
   p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
   p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
+  p.f16 = dt == FA_F16;
   p.scale = scale; p.causal = causal; p.cu = cu;
   p.wait_limit_ns = g_wait_limit_ns.load();
   g_detail[0] = 0;
@@ -220,6 +221,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.q = q; p.k = k; p.v = v; p.o = const_cast<void*>(o); p.lse = const_cast<float*>(lse);
   p.dout = dout; p.dq = dq; p.dk = dk; p.dv = dv;
   p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
+  p.f16 = dt == FA_F16;
   p.scale = scale; p.causal = causal; p.cu = cu;
   p.wait_limit_ns = g_wait_limit_ns.load();
   const long long rows = p.rows();

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,6 +39,7 @@ struct Problem {
   float* dq_acc;    // float32 dQ accumulator (backward, tensor-core path)
   int B, H, N, D;
   int T;            // packed token count (0 when dense)
+  int f16;          // 16-bit tensors: 1 = fp16, 0 = bf16
   float scale;
   int causal;
   const int32_t* cu;  // device pointer or nullptr
@@ -93,8 +95,10 @@ __device__ __forceinline__ GridItem grouped_heavy_first(int target_heads) {
 
 __device__ __forceinline__ float ld_elem(const float* p, long long i) { return p[i]; }
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float ld_elem(const __half* p, long long i) { return __half2float(p[i]); }
 __device__ __forceinline__ void st_elem(float* p, long long i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, long long i, float x) { p[i] = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void st_elem(__half* p, long long i, float x) { p[i] = __float2half_rn(x); }
 
 // Counts kernel launches (read by fa_launch_count); every launcher bumps it.
 void note_launches(unsigned n);

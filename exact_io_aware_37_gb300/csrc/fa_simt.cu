@@ -297,11 +297,13 @@ cudaError_t dispatch_bwd(const Problem& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_simt_fwd(const Problem& p, fa_dtype dt, cudaStream_t s) {
-  return dt == FA_F32 ? dispatch_fwd<float>(p, s) : dispatch_fwd<__nv_bfloat16>(p, s);
+  return dt == FA_F32 ? dispatch_fwd<float>(p, s)
+                       : dt == FA_F16 ? dispatch_fwd<__half>(p, s) : dispatch_fwd<__nv_bfloat16>(p, s);
 }
 
 cudaError_t launch_simt_bwd(const Problem& p, fa_dtype dt, cudaStream_t s) {
-  return dt == FA_F32 ? dispatch_bwd<float>(p, s) : dispatch_bwd<__nv_bfloat16>(p, s);
+  return dt == FA_F32 ? dispatch_bwd<float>(p, s)
+                       : dt == FA_F16 ? dispatch_bwd<__half>(p, s) : dispatch_bwd<__nv_bfloat16>(p, s);
 }
 
 cudaError_t launch_bwd_preprocess(const Problem& p, fa_dtype dt, bool zero_dq_acc, cudaStream_t s) {
@@ -310,6 +312,8 @@ cudaError_t launch_bwd_preprocess(const Problem& p, fa_dtype dt, bool zero_dq_ac
   const long long blocks = (rows * 32 + 255) / 256;
   if (dt == FA_F32)
     bwd_preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(p, rows, zero_dq_acc ? 1 : 0);
+  else if (dt == FA_F16)
+    bwd_preprocess_kernel<__half><<<(unsigned)blocks, 256, 0, s>>>(p, rows, zero_dq_acc ? 1 : 0);
   else
     bwd_preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(p, rows, zero_dq_acc ? 1 : 0);
   note_launches(1);

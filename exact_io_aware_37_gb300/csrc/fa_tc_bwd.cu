@@ -53,7 +53,7 @@ struct BwdParams {
   const float* lse;
   const float* dvec;
   float* dq_acc;
-  __nv_bfloat16* dk;
+  __nv_bfloat16* dk;  // 16-bit storage: bf16 or fp16 per F16
   __nv_bfloat16* dv;
   const int32_t* cu;
   unsigned* status;
@@ -93,7 +93,7 @@ struct BwdCfg {
   static_assert(kSmemBytes <= 232448, "backward tiles exceed the shared-memory limit");
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // P^T as bf16 pairs into this half's first 32 score columns (already read)
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
         tmem_st32(t_s, pk);
         tmem_st_wait();
       }
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           const int c = c8 * 8 + 2 * e;
           const float d0 = pr[c] * (__uint_as_float(sv[c >> 5][c & 31]) - sd[c]);
           const float d1 = pr[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - sd[c + 1]);
-          u[e] = pack_bf16x2(d0, d1);
+          u[e] = pack16x2<F16>(d0, d1);
         }
         // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
         *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
@@ -311,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-              u.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-              u.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-              u.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+              u.x = pack16x2<F16>(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+              u.y = pack16x2<F16>(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+              u.z = pack16x2<F16>(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+              u.w = pack16x2<F16>(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
               dst[v4] = u;
             }
           }
@@ -382,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t id_nn = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK: A K-major, B MN-major
+      const uint32_t id_nn = idesc16<F16>(128, 128, false, false);  // S^T, dP^T
+      const uint32_t id_acc = idesc16<F16>(128, D, false, true);    // dV, dK: A K-major, B MN-major
       // dQ^T = K^T dS^T (M = D) or dQ = dS K (N = D): A and B both MN-major
-      const uint32_t id_dq = C::kDqTransposed ? idesc_bf16(128, 128, true, true) : idesc_bf16(128, D, true, true);
+      const uint32_t id_dq = C::kDqTransposed ? idesc16<F16>(128, 128, true, true) : idesc16<F16>(128, D, true, true);
       const uint32_t sk = smem_u32(smem + C::kKOff), sv = smem_u32(smem + C::kVOff);
       const uint32_t sq = smem_u32(smem + C::kQOff), sdo = smem_u32(smem + C::kDOOff);
       const uint32_t sds = smem_u32(smem + C::kDSOff);
@@ -487,22 +487,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// dQ = bf16(scale * dQ_acc), four elements per thread.
+// dQ = scale * dQ_acc rounded to the 16-bit input type, four elements per thread.
+template <bool F16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
                                                          long long n4, float scale) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 a = acc[i];
-    dq[i] = make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
+    dq[i] = make_uint2(pack16x2<F16>(a.x * scale, a.y * scale), pack16x2<F16>(a.z * scale, a.w * scale));
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   using C = BwdCfg<D>;
   BwdParams bp;
-  if (!make_bf16_map(&bp.tq, p.q, p, kBM) || !make_bf16_map(&bp.tk, p.k, p, kBN) ||
-      !make_bf16_map(&bp.tv, p.v, p, kBN) || !make_bf16_map(&bp.tdo, p.dout, p, kBM))
+  if (!make_map16(&bp.tq, p.q, p, kBM) || !make_map16(&bp.tk, p.k, p, kBN) ||
+      !make_map16(&bp.tv, p.v, p, kBN) || !make_map16(&bp.tdo, p.dout, p, kBM))
     return note_error("backward tensor map encode", cudaErrorInvalidValue);
   bp.lse = p.lse;
   bp.dvec = p.dvec;
@@ -519,10 +520,10 @@ cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   bp.c2 = p.scale * kLog2e;
   bp.scale = p.scale;
   bp.causal = p.causal;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kBN - 1) / kBN, p.H, p.B);
-  tc_bwd_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
+  tc_bwd_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }
@@ -534,15 +535,19 @@ cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s) {
   const long long n4 = p.rows() * D / 4;
   const long long want = (n4 + 255) / 256;
   const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
-  dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(p.dq_acc), static_cast<uint2*>(p.dq), n4,
-                                           p.scale);
+  const float4* acc = reinterpret_cast<const float4*>(p.dq_acc);
+  uint2* dq = static_cast<uint2*>(p.dq);
+  if (p.f16)
+    dq_convert_kernel<true><<<blocks, 256, 0, s>>>(acc, dq, n4, p.scale);
+  else
+    dq_convert_kernel<false><<<blocks, 256, 0, s>>>(acc, dq, n4, p.scale);
   note_launches(1);
   return note_error("dq convert launch", cudaGetLastError());
 }
 
 
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s) {
-  if (p.D == 64) return launch_bwd_d<64>(p, s);
+  if (p.D == 64) return p.f16 ? launch_bwd_d<64, true>(p, s) : launch_bwd_d<64, false>(p, s);
   if (p.D == 128) return launch_tc_bwd128(p, s);
   return cudaErrorInvalidValue;
 }

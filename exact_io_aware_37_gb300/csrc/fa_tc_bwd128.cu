@@ -65,7 +65,7 @@ struct Bwd128Params {
   const float* lse;
   const float* dvec;
   float* dq_acc;
-  __nv_bfloat16* dk;
+  __nv_bfloat16* dk;  // 16-bit storage: bf16 or fp16 per F16
   __nv_bfloat16* dv;
   const int32_t* cu;
   unsigned* status;
@@ -93,6 +93,7 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
 
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_constant__ Bwd128Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
         tmem_st32(t_s, pk);
         tmem_st_wait();
       }
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           fsub2(t0, t1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
                 dv[2 * e], dv[2 * e + 1]);
           fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
-          dsp[4 * c8 + e] = pack_bf16x2(d0, d1);
+          dsp[4 * c8 + e] = pack16x2<F16>(d0, d1);
         }
       }
       tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
@@ -308,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-              u.y = pack_bf16x2(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-              u.z = pack_bf16x2(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-              u.w = pack_bf16x2(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+              u.x = pack16x2<F16>(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+              u.y = pack16x2<F16>(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+              u.z = pack16x2<F16>(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+              u.w = pack16x2<F16>(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
               dst[v4] = u;
             }
           }
@@ -404,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       bulk_wait_all();
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t id_nn = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
-      const uint32_t id_acc = idesc_bf16(128, D, false, true);    // dV, dK: B MN-major
-      const uint32_t id_dq = idesc_bf16(128, 128, true, true);    // dQ^T: both MN-major
+      const uint32_t id_nn = idesc16<F16>(128, 128, false, false);  // S^T, dP^T: both K-major
+      const uint32_t id_acc = idesc16<F16>(128, D, false, true);    // dV, dK: B MN-major
+      const uint32_t id_dq = idesc16<F16>(128, 128, true, true);    // dQ^T: both MN-major
       // Descriptors, advanced by adding (byte offset >> 4) to the start field.
       // k* = K-major view, m* = MN-major view of the same tile.
       const uint64_t kK = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);
@@ -508,10 +509,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
+template <bool F16>
+cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   Bwd128Params bp;
-  if (!make_bf16_map(&bp.tq, p.q, p, kTile) || !make_bf16_map(&bp.tk, p.k, p, kTile) ||
-      !make_bf16_map(&bp.tv, p.v, p, kTile) || !make_bf16_map(&bp.tdo, p.dout, p, kTile))
+  if (!make_map16(&bp.tq, p.q, p, kTile) || !make_map16(&bp.tk, p.k, p, kTile) ||
+      !make_map16(&bp.tv, p.v, p, kTile) || !make_map16(&bp.tdo, p.dout, p, kTile))
     return note_error("backward tensor map encode", cudaErrorInvalidValue);
   bp.lse = p.lse;
   bp.dvec = p.dvec;
@@ -528,12 +530,16 @@ cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
   bp.c2 = p.scale * kLog2e;
   bp.scale = p.scale;
   bp.causal = p.causal;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kTile - 1) / kTile, p.H, p.B);
-  tc_bwd128_kernel<<<grid, kThreads, kSmemBytes, s>>>(bp);
+  tc_bwd128_kernel<F16><<<grid, kThreads, kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
+}
+
+cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
+  return p.f16 ? launch_bwd128_t<true>(p, s) : launch_bwd128_t<false>(p, s);
 }
 
 }  // namespace fa

@@ -54,7 +54,7 @@ constexpr int kFwdHeadGroup = 16;  // heads per group of the causal block order 
 
 struct FwdParams {
   CUtensorMap tq, tk, tv;
-  __nv_bfloat16* o;
+  __nv_bfloat16* o;  // 16-bit storage: bf16 or fp16 per F16
   float* lse;
   const int32_t* cu;
   unsigned* status;
@@ -80,7 +80,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             const float p0 = ex2_approx(a0);
             const float p1 = ex2_approx(a1);
             fadd2(rs0, rs1, p0, p1);
-            pk[c] = pack_bf16x2(p0, p1);
+            pk[c] = pack16x2<F16>(p0, p1);
           }
           tmem_st32(t_s + 32 * hf, pk);
         }
@@ -256,10 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-              u.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-              u.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-              u.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+              u.x = pack16x2<F16>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+              u.y = pack16x2<F16>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+              u.z = pack16x2<F16>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+              u.w = pack16x2<F16>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
               dst[v4] = u;
             }
           }
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t id_s = idesc_bf16(kBM, kBN, false, false);
-      const uint32_t id_o = idesc_bf16(kBM, D, false, true);
+      const uint32_t id_s = idesc16<F16>(kBM, kBN, false, false);
+      const uint32_t id_o = idesc16<F16>(kBM, D, false, true);
       // Descriptors are built once and advanced by adding (byte offset >> 4)
       // to their start-address field.
       const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
@@ -417,12 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   using C = FwdCfg<D>;
   FwdParams fp;
-  if (!make_bf16_map(&fp.tq, p.q, p, kBM) || !make_bf16_map(&fp.tk, p.k, p, kBN) ||
-      !make_bf16_map(&fp.tv, p.v, p, kBN))
+  if (!make_map16(&fp.tq, p.q, p, kBM) || !make_map16(&fp.tk, p.k, p, kBN) ||
+      !make_map16(&fp.tv, p.v, p, kBN))
     return note_error("forward tensor map encode", cudaErrorInvalidValue);
   fp.o = static_cast<__nv_bfloat16*>(p.o);
   fp.lse = p.lse;
@@ -435,11 +435,11 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   fp.T = p.T;
   fp.c2 = p.scale * kLog2e;
   fp.causal = p.causal;
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("forward smem attribute", e);
   const int n_qt = (p.N + kBM - 1) / kBM;
   dim3 grid((n_qt + 1) / 2, p.H, p.B);
-  tc_fwd_kernel<D><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
+  tc_fwd_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
   note_launches(1);
   return note_error("forward launch", cudaGetLastError());
 }
@@ -447,8 +447,8 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s) {
-  if (p.D == 64) return launch_fwd_d<64>(p, s);
-  if (p.D == 128) return launch_fwd_d<128>(p, s);
+  if (p.D == 64) return p.f16 ? launch_fwd_d<64, true>(p, s) : launch_fwd_d<64, false>(p, s);
+  if (p.D == 128) return p.f16 ? launch_fwd_d<128, true>(p, s) : launch_fwd_d<128, false>(p, s);
   return cudaErrorInvalidValue;
 }
 

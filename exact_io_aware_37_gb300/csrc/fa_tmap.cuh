@@ -26,12 +26,12 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// A bf16 attention tensor viewed as a 3-D array (D, rows, slabs):
+// A 16-bit (bf16 or fp16, from p.f16) attention tensor viewed as a 3-D array (D, rows, slabs):
 //   dense  [B, H, N, D]: rows = N, slabs = B * H;
 //   packed [H, T, D]   : rows = T, slabs = H.
 // Boxes are 64 columns (128 bytes, one 128-byte swizzle row) x box_rows rows
 // of one slab; rows past the slab's end read as zero.
-inline bool make_bf16_map(CUtensorMap* map, const void* base, const Problem& p, int box_rows) {
+inline bool make_map16(CUtensorMap* map, const void* base, const Problem& p, int box_rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const uint64_t rows = p.cu ? (uint64_t)p.T : (uint64_t)p.N;
@@ -40,7 +40,7 @@ inline bool make_bf16_map(CUtensorMap* map, const void* base, const Problem& p, 
   cuuint64_t strides[2] = {(cuuint64_t)p.D * 2, (cuuint64_t)p.D * 2 * rows};
   cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = enc(map, p.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -361,9 +361,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format;
 //   bit 15 A major (0 = K, 1 = MN); bit 16 B major; 17-22 N >> 3; 24-28 M >> 4.
+// A and B have one type (F16: both fp16, else both bf16), D is fp32.
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+  return idesc16<false>(M, N, a_mn_major, b_mn_major);
 }
 
 // Pack two fp32 into a bf16x2 word (round to nearest even); `lo` lands in
@@ -372,6 +377,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// The same for fp16x2.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (F16)
+    return pack_f16x2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
 }
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).

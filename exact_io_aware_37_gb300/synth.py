@@ -13,7 +13,7 @@ import torch
 
 SEED_Q, SEED_K, SEED_V, SEED_DO, SEED_LENS = 0, 1, 2, 3, 4
 
-DTYPES = {"bf16": torch.bfloat16, "f32": torch.float32}
+DTYPES = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 
 
 def normal(shape, seed, dtype, std=1.0):

@@ -30,6 +30,11 @@
  *          fp32 for softmax; head width D must be 64 or 128.
  *        FA_F32  -- all of them float32; arithmetic is fp32 FMA (no TF32);
  *          D must be 32, 64 or 128.
+ *        FA_F16  -- as FA_BF16 with IEEE half precision tensors (fp16 x fp16
+ *          -> fp32 tensor-core products; P and dS are rounded to fp16 before
+ *          their products); D must be 64 or 128.  (The 16-bit input type
+ *          of nexusofnerds.com "FlashAttention"; the pages give no separate
+ *          tolerance for it.)
  *        lse is always float32.
  *
  * Ownership and memory: every pointer argument is a DEVICE pointer owned by the
@@ -67,7 +72,7 @@ typedef enum {
   FA_ERR_WORKSPACE = -6     /* workspace NULL, misaligned or smaller than fa_bwd_workspace_size */
 } fa_status;
 
-typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+typedef enum { FA_BF16 = 0, FA_F32 = 1, FA_F16 = 2 } fa_dtype;
 
 /*
  * Forward pass.  tensortonic.com "FlashAttention" sections 5-7.

@@ -60,6 +60,7 @@ def test_forward_argument_validation(lib):
     assert _fwd(lib, D=64, dt=1) != UNSUPPORTED or True
     assert _fwd(lib, D=48, dt=1) == UNSUPPORTED
     assert _fwd(lib, dt=7) == UNSUPPORTED
+    assert _fwd(lib, D=32, dt=2) == UNSUPPORTED     # fp16 runs on the tensor cores only: D 64 or 128
     assert _fwd(lib, B=-1) == INVALID
     assert _fwd(lib, N=-5) == INVALID
     assert _fwd(lib, scale=float("nan")) == INVALID
@@ -99,6 +100,8 @@ def test_workspace_size(lib):
     assert f(2, 32, 4096, 128, None, 0, 0) == 2 * 32 * 4096 * 4 + 2 * 32 * 4096 * 128 * 4
     # packed: rows = H * T, rounded up to 256 bytes per part
     assert f(16, 32, 8192, 128, 0x1000, 1001, 0) == (32 * 1001 * 4 + 255) // 256 * 256 + 32 * 1001 * 128 * 4
+    # fp16 uses the same tensor-core path and workspace as bf16
+    assert f(2, 32, 4096, 128, None, 0, 2) == f(2, 32, 4096, 128, None, 0, 0)
     # float32 path needs only the D vector
     assert f(1, 1, 128, 64, None, 0, 1) == 512
     assert f(-1, 1, 1, 64, None, 0, 0) == 0
@@ -110,6 +113,8 @@ def test_strerror_and_path_names(lib):
     assert lib.fa_path_name(1, 64) == b"simt_f32"
     assert lib.fa_path_name(0, 96) is None
     assert lib.fa_path_name(0, 128) is not None
+    assert lib.fa_path_name(2, 64) == lib.fa_path_name(0, 64) == b"tcgen05"
+    assert lib.fa_path_name(2, 32) is None
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

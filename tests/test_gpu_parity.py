@@ -59,6 +59,19 @@ def test_tiny_f32_workload(causal):
     compare(torch.float32, {n: f64(t) for n, t in got.items()}, ref, f"tiny f32 causal={causal}")
 
 
+F16_CASES = [(2, 3, 17, 64), (2, 2, 300, 64), (1, 2, 256, 128), (1, 1, 513, 128), (3, 6, 384, 128)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", F16_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_dense_f16(shape, causal):
+    q, k, v, do = synth.qkv_do(shape, torch.float16, seed_offset=10)
+    scale = default_scale(shape[-1])
+    got = run(q, k, v, do, causal, scale)
+    ref = _dense_ref(q, k, v, do, scale, causal)
+    compare(torch.float16, {n: f64(t) for n, t in got.items()}, ref, f"f16 dense {shape} causal={causal}")
+
+
 @pytest.mark.parametrize("D", [32, 128])
 def test_f32_other_widths(D):
     q, k, v, do = synth.qkv_do((1, 2, 200, D), torch.float32, seed_offset=20)
@@ -68,20 +81,21 @@ def test_f32_other_widths(D):
     compare(torch.float32, {n: f64(t) for n, t in got.items()}, ref, f"f32 D={D}")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [64, 128])
-def test_packed_bf16(D, causal):
+def test_packed_16bit(D, causal, dtype):
     lengths = [1, 127, 128, 129, 300, 0, 5, 256]
     cu = synth.cu_seqlens(lengths)
     T = int(cu[-1])
-    q, k, v, do = synth.qkv_do((2, T, D), torch.bfloat16, seed_offset=30)
+    q, k, v, do = synth.qkv_do((2, T, D), dtype, seed_offset=30)
     scale = default_scale(D)
     got = run(q, k, v, do, causal, scale, cu=cu, max_seqlen=max(lengths))
     qn, kn, vn, don = (x.double().numpy() for x in (q, k, v, do))
     O, L = oracle.forward_varlen(qn, kn, vn, cu, scale, causal)
     dQ, dK, dV, _ = oracle.backward_varlen(qn, kn, vn, don, cu, scale, causal)
-    compare(torch.bfloat16, {n: f64(t) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
-            f"packed D={D} causal={causal}")
+    compare(dtype, {n: f64(t) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+            f"packed {dtype} D={D} causal={causal}")
 
 
 def test_causal_rows_ignore_future_keys():
