@@ -31,4 +31,7 @@ from .attention import (  # noqa: F401
     backward_head_blocked,
     online_softmax_row,
     tiled_forward_head,
+    cached_score_matrix,
+    forward_cached_head,
+    forward_cached,
 )

@@ -33,6 +33,11 @@ none of them re-types the formula below):
   online_softmax_row             the printed [1, 2, 3, 4] split-tile example in
                                  closed form; equal to the full-row softmax.
   tiled_forward_head             equal to forward_head for several tile sizes.
+  cached_score_matrix,           torch SDPA (float64) with the bottom-right
+  forward_cached_head,           boolean mask; with nq == nk equal to
+  forward_cached                 forward_head; row i equal to the unmasked
+                                 forward_head over keys 0 .. nk - nq + i; rows
+                                 with no allowed key give O = 0, L = -inf.
 No function is "parity unpinned".
 """
 
@@ -157,6 +162,54 @@ def backward(q, k, v, do, scale, causal):
             dQ[b, h], dK[b, h], dV[b, h], Dv[b, h] = backward_head(
                 q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
     return dQ, dK, dV, Dv
+
+
+# --------------------------------------------------------------------------
+# Cached decoding: nq new queries against nk keys and values already in the
+# cache (tensortonic.com "FlashAttention" section 8: a cached generation step
+# may have a single new query and a long set of past keys and values; section
+# 9: the newest query must be aligned with its actual position in the key
+# cache, so the square causal mask does not apply when the lengths differ).
+# --------------------------------------------------------------------------
+
+def cached_score_matrix(q, k, scale, causal):
+    """S = scale * Q K^T for nq queries that are the last nq positions of an
+    nk-long sequence: query i sits at position nk - nq + i, so causal allows
+    key j iff j <= i + (nk - nq) (the mask aligned at the bottom right).  For
+    nq == nk this is score_matrix's square mask.  When nq > nk the first
+    nq - nk rows have no allowed key.  Masked entries are -inf.
+    """
+    q = _f64(q)
+    k = _f64(k)
+    s = scale * (q @ k.T)
+    if causal:
+        nq, nk = s.shape
+        i = np.arange(nq)[:, None]
+        j = np.arange(nk)[None, :]
+        s = np.where(j <= i + (nk - nq), s, -np.inf)
+    return s
+
+
+def forward_cached_head(q, k, v, scale, causal):
+    """One head of a cached decoding step: (O [nq, d], L [nq]), by the same
+    definition as forward_head (softmax of the masked scores, times V);
+    rows without an allowed key get O = 0, L = -inf."""
+    s = cached_score_matrix(q, k, scale, causal)
+    P, L, _, _ = _softmax_rows(s)
+    return P @ _f64(v), L
+
+
+def forward_cached(q, k, v, scale, causal):
+    """Dense cached step: q [B, H, nq, D], k and v [B, H, nk, D] ->
+    (O [B, H, nq, D], L [B, H, nq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, nq, _ = q.shape
+    O = np.zeros((B, H, nq, v.shape[-1]))
+    L = np.zeros((B, H, nq))
+    for b in range(B):
+        for h in range(H):
+            O[b, h], L[b, h] = forward_cached_head(q[b, h], k[b, h], v[b, h], scale, causal)
+    return O, L
 
 
 def _segments(cu_seqlens):

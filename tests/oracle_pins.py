@@ -215,6 +215,51 @@ def check_gradient_invariants(impl):
         np.testing.assert_allclose(D, (do * O).sum(1), atol=1e-13)
 
 
+def check_cached_decoding(impl):
+    """Bottom-right aligned cached step: against torch SDPA with an explicit
+    boolean mask (float64); the square case equals forward_head; every row
+    equals an unmasked head over its visible key prefix; rows with no key
+    give O = 0 and L = -inf; the batched wrapper matches the per-head one."""
+    import torch
+    r = _rng(19)
+    for nq, nk, d in ((1, 9, 4), (3, 11, 5), (6, 6, 3), (5, 2, 4)):
+        q = r.standard_normal((nq, d))
+        k, v = r.standard_normal((2, nk, d))
+        scale = 0.7
+        O, L = impl.forward_cached_head(q, k, v, scale, True)
+        allowed = np.arange(nk)[None, :] <= np.arange(nq)[:, None] + (nk - nq)
+        for i in range(nq):
+            vis = int(allowed[i].sum())
+            if vis == 0:
+                assert np.all(O[i] == 0.0) and L[i] == -np.inf
+                continue
+            Oi, Li = impl.forward_head(q[i:i + 1], k[:vis], v[:vis], scale, False)
+            np.testing.assert_allclose(O[i], Oi[0], atol=1e-13)
+            np.testing.assert_allclose(L[i], Li[0], atol=1e-13)
+        rows = allowed.any(1)
+        if rows.any():
+            t = torch.nn.functional.scaled_dot_product_attention(
+                torch.tensor(q[rows])[None], torch.tensor(k)[None], torch.tensor(v)[None],
+                attn_mask=torch.tensor(allowed[rows])[None], scale=scale)[0].numpy()
+            np.testing.assert_allclose(O[rows], t, atol=1e-12)
+        if nq == nk:
+            Of, Lf = impl.forward_head(q, k, v, scale, True)
+            np.testing.assert_allclose(O, Of, atol=1e-13)
+            np.testing.assert_allclose(L, Lf, atol=1e-13)
+        On, _ = impl.forward_cached_head(q, k, v, scale, False)
+        Ofull, _ = impl.forward_head(q, k, v, scale, False) if nq == nk else (None, None)
+        if Ofull is not None:
+            np.testing.assert_allclose(On, Ofull, atol=1e-13)
+    qb = r.standard_normal((2, 3, 2, 4))
+    kb, vb = r.standard_normal((2, 2, 3, 7, 4))
+    Ob, Lb = impl.forward_cached(qb, kb, vb, 0.5, True)
+    for b in range(2):
+        for h in range(3):
+            Oh, Lh = impl.forward_cached_head(qb[b, h], kb[b, h], vb[b, h], 0.5, True)
+            np.testing.assert_allclose(Ob[b, h], Oh, atol=0)
+            np.testing.assert_allclose(Lb[b, h], Lh, atol=0)
+
+
 ALL_CHECKS = [
     check_split_tile_example,
     check_zero_query,
@@ -225,4 +270,5 @@ ALL_CHECKS = [
     check_torch_sdpa,
     check_finite_differences,
     check_gradient_invariants,
+    check_cached_decoding,
 ]

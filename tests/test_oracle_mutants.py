@@ -17,8 +17,10 @@ import oracle.attention as attention
 import oracle_pins
 
 MUTANTS = {
-    "scores_drop_scale": ("    s = scale * (q @ k.T)\n    if causal:",
-                          "    s = (q @ k.T)\n    if causal:"),
+    "scores_drop_scale": ("    s = scale * (q @ k.T)\n    if causal:\n        i = np.arange(s.shape[0])",
+                          "    s = (q @ k.T)\n    if causal:\n        i = np.arange(s.shape[0])"),
+    "cached_scores_drop_scale": ("    s = scale * (q @ k.T)\n    if causal:\n        nq, nk = s.shape",
+                                 "    s = (q @ k.T)\n    if causal:\n        nq, nk = s.shape"),
     "mask_strict_lower": ("        s = np.where(j <= i, s, -np.inf)\n    return s",
                           "        s = np.where(j < i, s, -np.inf)\n    return s"),
     "mask_upper": ("        s = np.where(j <= i, s, -np.inf)\n    return s",
@@ -49,6 +51,14 @@ MUTANTS = {
                     "    D = dP.sum(axis=1)\n    dS = P"),
     "dV_missing_transpose": ("    dV = P.T @ do\n    dP = do @ v.T",
                              "    dV = P @ do\n    dP = do @ v.T"),
+    "cached_mask_top_left": ("        s = np.where(j <= i + (nk - nq), s, -np.inf)",
+                             "        s = np.where(j <= i, s, -np.inf)"),
+    "cached_mask_off_by_one": ("        s = np.where(j <= i + (nk - nq), s, -np.inf)",
+                               "        s = np.where(j < i + (nk - nq), s, -np.inf)"),
+    "cached_mask_sign": ("        s = np.where(j <= i + (nk - nq), s, -np.inf)",
+                         "        s = np.where(j <= i - (nk - nq), s, -np.inf)"),
+    "cached_output_values_swapped": ("    return P @ _f64(v), L\n",
+                                     "    return P @ _f64(k), L\n"),
     "dP_transposed": ("    dV = P.T @ do\n    dP = do @ v.T",
                       "    dV = P.T @ do\n    dP = v @ do.T"),
 }
