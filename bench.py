@@ -43,6 +43,8 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 TRAFFIC_BY_SOURCE = {
     # tc_bwd128_kernel, B2 H32 N4096 D128 causal: 404.8 MB read + 220.6 MB written
     "0aa74a94bebafe9c7ba8877e237e809dc18ec8ded1dba952993288f920bf8c54": 625.5e6,
+    # decode_split_kernel, B16 H32 nq1 nk8192 D128: 2147.7 MB read + 3.9 MB written
+    "690b84cb5610de6d23e66e577f0baf49ac3373182539be7030411dc3bd37a5e8": 2151.6e6,
 }
 
 
@@ -58,6 +60,11 @@ def peaks():
             p = json.load(f)
         return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
     return FALLBACK_PEAK_TFLOPS, 6800.0, "fallback"
+
+
+def hbm_peak():
+    _, gbs, kind = peaks()
+    return gbs, f"HBM copy, {kind}"
 
 
 class ClockSampler:
@@ -217,6 +224,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="16-bit input type (the same synthetic draws, rounded to it)")
+    ap.add_argument("--workload", choices=["train", "decode"], default="train",
+                    help="train: causal fwd+bwd at B2 H32 N4096 D128 (the default); "
+                         "decode: one cached decoding step, B16 H32, 1 query, 8192 keys, D128")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -231,6 +241,9 @@ def main():
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.workload == "decode":
+        bench_decode(fa, synth, args, dist, rank, world, local, device)
+        return
     cfg = dict(synth.WORKLOADS[WORKLOAD], dtype=args.dtype)
     q_h, k_h, v_h, do_h = synth.make_dense(cfg)
     B, H, N, D = q_h.shape
@@ -332,6 +345,101 @@ def main():
     barrier(dist)
     if dist is not None:
         dist.destroy_process_group()
+
+
+DECODE_WORKLOAD = "decode_b16h32q1k8192d128"
+
+
+def bench_decode(fa, synth, args, dist, rank, world, local, device):
+    """One cached decoding step per timed iteration (fa_decode: split-KV pass +
+    merge).  The cache (K, V: 2.1 GB, larger than L2) is resident; the metric
+    is algorithmic HBM bytes (K, V, q, o, lse) per second, against the measured
+    copy bandwidth."""
+    cfg = dict(synth.WORKLOADS[DECODE_WORKLOAD], dtype=args.dtype)
+    q_h, k_h, v_h = synth.make_decode(cfg)
+    B, H, nq, D = q_h.shape
+    nk = k_h.shape[2]
+    scale = 1.0 / D ** 0.5
+    q, k, v = (x.to(device) for x in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, nq), dtype=torch.float32, device=device)
+    ws_bytes = fa.fa_decode_workspace_size(q, k)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device) if ws_bytes else None
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        fa.fa_decode(q, k, v, o, lse, True, scale, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
+    launches0 = fa.fa_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier(dist)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fa.fa_decode(q, k, v, o, lse, True, scale, workspace=ws, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    launches = fa.fa_launch_count() - launches0
+    assert fa.fa_get_last_device_error() == 0
+    ms = max_over_ranks(dist, a.elapsed_time(b), device) / args.steps
+    elem = q.element_size()
+    step_bytes = (2 * B * H * nk * D + 2 * B * H * nq * D) * elem + B * H * nq * 4
+    gbs = world * step_bytes / (ms * 1e-3) / 1e9
+    peak_gbs, peak_kind = hbm_peak()
+
+    # end to end: the step's new query (and the new token's K / V rows, which a
+    # caller appends to the cache) come from pinned host memory; o and lse go back
+    hq = q_h.pin_memory()
+    hkv = [x[:, :, -nq:].contiguous().pin_memory() for x in (k_h, v_h)]
+    dkv = [torch.empty_like(x, device=device) for x in hkv]  # contiguous staging, then appended on the device
+    ho, hl = torch.empty_like(q_h).pin_memory(), torch.empty((B, H, nq), dtype=torch.float32).pin_memory()
+    steps = max(10, args.steps // 4)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        for hs, ds, cache in zip(hkv, dkv, (k, v)):
+            ds.copy_(hs, non_blocking=True)
+            cache[:, :, -nq:].copy_(ds)
+        fa.fa_decode(q, k, v, o, lse, True, scale, workspace=ws, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(dist)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, a.elapsed_time(b), device) / steps
+    h2d = (hq.numel() + hkv[0].numel() + hkv[1].numel()) * elem
+    d2h = ho.numel() * elem + hl.numel() * 4
+    if rank != 0:
+        return
+    line = {
+        "metric": f"cached decoding step, algorithmic HBM GB/s ({args.dtype})", "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "B": B, "H": H, "nq": nq, "nk": nk, "D": D, "causal": True,
+                   "kernel_path": "simt split-KV + merge" if ws_bytes else "simt split-KV (one split)",
+                   "l2": f"K/V cache {2 * k.numel() * elem / 2**30:.1f} GiB > 129 MiB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peak_gbs, "unit": "GB/s",
+                     "frac": gbs / world / peak_gbs, "kernel": "decode_split_kernel",
+                     "traffic": TRAFFIC_BY_SOURCE.get(kernel_source_sha(
+                         os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc", "fa_decode.cu"))),
+                     "peak_kind": peak_kind, "bytes_per_step": step_bytes},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    print(json.dumps(line), flush=True)
 
 
 def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, args):

@@ -19,7 +19,7 @@ from ._lib import FA_BF16, FA_F16, FA_F32, FAError, lib, library_path  # noqa: F
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
            "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
-           "FAError"]
+           "fa_decode", "fa_decode_workspace_size", "decode", "FAError"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.float16: FA_F16}
 
@@ -149,6 +149,42 @@ def fa_bwd_static_ws(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_s
 
 
 STATIC_WS_BYTES = 16 << 20
+
+
+def fa_decode_workspace_size(q, k):
+    """Bytes of scratch fa_decode needs for q [B, H, nq, D] against k [B, H, nk, D]."""
+    B, H, nq, D = q.shape
+    return int(lib().fa_decode_workspace_size(B, H, nq, k.shape[2], D, _DT[q.dtype]))
+
+
+def fa_decode(q, k, v, o, lse, causal, scale=None, workspace=None, stream=None):
+    """Enqueue a cached decoding step: q [B, H, nq, D] against the cache
+    k, v [B, H, nk, D]; query i is at position nk - nq + i.  Writes o (dtype of
+    q) and lse [B, H, nq] (float32)."""
+    _check(q, k, v, o, lse)
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q must be [B, H, nq, D] and k, v [B, H, nk, D]")
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    B, H, nq, D = q.shape
+    nk = k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = fa_decode_workspace_size(q, k)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, nq, nk, D, scale, int(bool(causal)),
+                         _DT[q.dtype], _ptr(workspace), nbytes, _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_decode")
+
+
+def decode(q, k, v, causal=True, scale=None, stream=None):
+    """Allocating convenience wrapper around fa_decode: returns (o, lse)."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_decode(q, k, v, o, lse, causal, scale, stream=stream)
+    return o, lse
 
 
 def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):

@@ -243,4 +243,43 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+size_t fa_decode_workspace_size(int B, int H, int nq, int nk, int D, fa_dtype dt) {
+  (void)dt;
+  if (B <= 0 || H <= 0 || nq <= 0 || nk < 0 || D <= 0) return 0;
+  return decode_workspace_bytes(B, H, nq, nk, D);
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int nq, int nk,
+                    int D, float scale, int causal, fa_dtype dt, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (B < 0 || H < 0 || nq < 0 || nk < 0) return FA_ERR_INVALID;
+  if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return FA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+  if (dt != FA_BF16 && dt != FA_F32 && dt != FA_F16) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)nq * B * H > (1ll << 31) - 1) return FA_ERR_UNSUPPORTED;  // merge grid
+  if (B == 0 || H == 0 || nq == 0) return FA_OK;
+  fa_status st;
+  for (const void* p : {q, (const void*)o})
+    if ((st = check_tensor(p)) != FA_OK) return st;
+  if (nk > 0)  // an empty cache has no K or V to point at
+    for (const void* p : {k, v})
+      if ((st = check_tensor(p)) != FA_OK) return st;
+  if (lse == nullptr) return FA_ERR_INVALID;
+  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  const size_t need = fa_decode_workspace_size(B, H, nq, nk, D, dt);
+  if (need > 0 && (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need)) return FA_ERR_WORKSPACE;
+
+  Problem p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.H = H; p.N = nq; p.D = D;
+  p.scale = scale; p.causal = causal;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  g_detail[0] = 0;
+  if (note_error("status word", status_word(&p.status)) != cudaSuccess) return FA_ERR_CUDA;
+  cudaError_t e = launch_decode(p, nq, nk, dt, workspace, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -121,4 +121,14 @@ cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s);  // main kernel onl
 cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s);  // main kernel only, D = 128
 cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s);  // dQ = bf16(scale * dQ_acc)
 
+// Cached decoding (fa_decode.cu).  Problem fields q, k, v, o, lse, B, H, D,
+// scale, causal are used; nq / nk are the query and cached-key counts.
+struct DecodeSplit {
+  int splits;          // key splits per (b, h)
+  int keys_per_split;
+};
+DecodeSplit decode_split(int B, int H, int nq, int nk);
+size_t decode_workspace_bytes(int B, int H, int nq, int nk, int D);
+cudaError_t launch_decode(const Problem& p, int nq, int nk, fa_dtype dt, void* workspace, cudaStream_t s);
+
 }  // namespace fa

@@ -58,6 +58,9 @@ WORKLOADS = {
                              dtype="bf16", std=1.0, causal=(True,)),
     "window_b1h32n32768d128": dict(B=1, H=32, N=32768, D=128, dtype="bf16",
                                    std=0.5, causal=(True,)),
+    # a cached decoding step: one new query per (b, h) against 8192 cached keys
+    "decode_b16h32q1k8192d128": dict(B=16, H=32, nq=1, nk=8192, D=128, dtype="bf16",
+                                     std=1.0, causal=(True,)),
 }
 
 
@@ -66,6 +69,16 @@ def make_dense(name_or_cfg, seed_offset=0):
     cfg = WORKLOADS[name_or_cfg] if isinstance(name_or_cfg, str) else name_or_cfg
     shape = (cfg["B"], cfg["H"], cfg["N"], cfg["D"])
     return qkv_do(shape, DTYPES[cfg["dtype"]], cfg.get("std", 1.0), seed_offset)
+
+
+def make_decode(name_or_cfg, seed_offset=0):
+    """CPU (q [B,H,nq,D], k, v [B,H,nk,D]) for a cached decoding workload."""
+    cfg = WORKLOADS[name_or_cfg] if isinstance(name_or_cfg, str) else name_or_cfg
+    dt, std = DTYPES[cfg["dtype"]], cfg.get("std", 1.0)
+    B, H, D = cfg["B"], cfg["H"], cfg["D"]
+    return (normal((B, H, cfg["nq"], D), SEED_Q + seed_offset, dt, std),
+            normal((B, H, cfg["nk"], D), SEED_K + seed_offset, dt, std),
+            normal((B, H, cfg["nk"], D), SEED_V + seed_offset, dt, std))
 
 
 def make_varlen(name_or_cfg, seed_offset=0):

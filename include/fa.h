@@ -220,6 +220,33 @@ void fa_bwd_time_main_kernel(void* start_event, void* stop_event);
  */
 unsigned long long fa_launch_count(void);
 
+/* Cached decoding step (tensortonic.com "FlashAttention" section 8: a
+ * generation step has a few new queries and a long set of cached keys and
+ * values; section 9: the newest query must be aligned with its actual position
+ * in the key cache).
+ *
+ *   q    [B, H, nq, D]  the new queries            (dtype, device)
+ *   k, v [B, H, nk, D]  the cache, including the entries of the new tokens
+ *                       (may be NULL when nk == 0)
+ *   o    [B, H, nq, D]  written (dtype);  lse [B, H, nq] float32, natural log
+ *
+ * Query row i sits at position nk - nq + i of the sequence, so causal allows
+ * key j iff j <= i + (nk - nq) (the square top-left mask of fa_fwd is the
+ * nq == nk case).  Rows with no allowed key (nq > nk, causal) get O = 0 and
+ * lse = -inf.  Any nq >= 1 is accepted; the kernel is built for nq <= 8 (one
+ * CTA serves up to 8 rows).  D must be 64 or 128; all three dtypes.  The work
+ * streams K and V once (HBM-bound): keys are split across CTAs and the partial
+ * states are merged by a second kernel (section 5's rescaling rule), in fp32.
+ *
+ * workspace: device scratch of fa_decode_workspace_size(...) bytes (0 when a
+ * single split suffices; then workspace may be NULL), 256-byte aligned, owned
+ * by the caller.  Errors: FA_ERR_INVALID / UNSUPPORTED / ALIGN / WORKSPACE
+ * before any launch, FA_ERR_CUDA if a launch fails.  Asynchronous on stream. */
+size_t fa_decode_workspace_size(int B, int H, int nq, int nk, int D, fa_dtype dtype);
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int nq, int nk,
+                    int D, float scale, int causal, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -117,6 +117,37 @@ def test_strerror_and_path_names(lib):
     assert lib.fa_path_name(2, 32) is None
 
 
+def test_decode_validation_and_workspace(lib):
+    def dec(ws=0x100000, ws_bytes=1 << 30, **kw):
+        a = dict(q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=2, nq=1, nk=1000, D=128, scale=0.1,
+                 causal=1, dt=0)
+        a.update(kw)
+        return lib.fa_decode(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["nq"], a["nk"], a["D"],
+                             a["scale"], a["causal"], a["dt"], ws, ws_bytes, None)
+    assert dec(D=96) == UNSUPPORTED
+    assert dec(D=32) == UNSUPPORTED
+    assert dec(dt=7) == UNSUPPORTED
+    assert dec(nq=-1) == INVALID
+    assert dec(nk=-1) == INVALID
+    assert dec(causal=2) == INVALID
+    assert dec(scale=float("nan")) == INVALID
+    assert dec(q=None) == INVALID
+    assert dec(lse=None) == INVALID
+    assert dec(k=0x1008) == ALIGN
+    assert dec(ws=None) == WORKSPACE
+    assert dec(ws=0x100010) == WORKSPACE
+    assert dec(ws_bytes=16) == WORKSPACE
+    assert dec(B=0) == OK and dec(nq=0) == OK
+    assert dec(k=None) == INVALID
+    assert dec(k=None, v=None, nk=0) != INVALID   # an empty cache needs no K / V (CUDA error without a GPU)
+    size = lib.fa_decode_workspace_size
+    # 1 x 2 heads, 1000 keys: four splits of 250 keys; per split and row D floats + (m, l)
+    assert size(1, 2, 1, 1000, 128, 0) == 4 * 2 * 128 * 4 + 256
+    # enough (b, h) pairs to fill the GPU: one split, no scratch
+    assert size(16, 64, 1, 8192, 128, 0) == 0
+    assert size(1, 1, 1, 100, 64, 0) == 0 and size(0, 1, 1, 100, 64, 0) == 0
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert _fwd(lib) == CUDA
