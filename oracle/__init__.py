@@ -34,4 +34,10 @@ from .attention import (  # noqa: F401
     cached_score_matrix,
     forward_cached_head,
     forward_cached,
+    philox4x32_10,
+    dropout_keep,
+    forward_head_dropout,
+    backward_head_dropout,
+    forward_dropout,
+    backward_dropout,
 )

@@ -38,6 +38,14 @@ none of them re-types the formula below):
   forward_cached                 forward_head; row i equal to the unmasked
                                  forward_head over keys 0 .. nk - nq + i; rows
                                  with no allowed key give O = 0, L = -inf.
+  philox4x32_10                  the published known-answer vectors of
+                                 Philox4x32-10 (three counter/key pairs).
+  dropout_keep                   keep fraction within binomial bounds;
+                                 independent of the row/column orientation.
+  forward_head_dropout,          p = 0 gives forward_head / backward_head;
+  backward_head_dropout,         torch autograd (float64) of the same masked
+  forward_dropout,               computation; central finite differences;
+  backward_dropout               D_i = rowsum(dO o O) with the dropped O.
 No function is "parity unpinned".
 """
 
@@ -161,6 +169,105 @@ def backward(q, k, v, do, scale, causal):
         for h in range(H):
             dQ[b, h], dK[b, h], dV[b, h], Dv[b, h] = backward_head(
                 q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+    return dQ, dK, dV, Dv
+
+
+# --------------------------------------------------------------------------
+# Attention dropout (tensortonic.com "FlashAttention" section 7: with dropout
+# the backward must reproduce the forward's dropout decisions from saved
+# random-number-generator information rather than sample a new mask).
+#
+# The decisions come from the counter-based generator Philox4x32-10 (Salmon,
+# Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011),
+# so any element's decision can be regenerated from (seed, position) alone:
+# element (i, j) of head bh (= b * H + h) takes 32-bit word j mod 4 of
+# Philox4x32-10 with counter (floor(j / 4), i, bh, offset) and key
+# (seed mod 2^32, seed div 2^32); it is kept iff word / 2^32 >= p.  Kept
+# weights are scaled by 1 / (1 - p): O = (P o Z) V / (1 - p).  L is that of the
+# undropped softmax.
+# --------------------------------------------------------------------------
+
+_PHILOX_M0, _PHILOX_M1 = 0xD2511F53, 0xCD9E8D57       # round multipliers
+_PHILOX_W0, _PHILOX_W1 = 0x9E3779B9, 0xBB67AE85       # key increments (Weyl sequence)
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32 with 10 rounds.  counter: four uint32 arrays (broadcastable),
+    key: two uint32 values.  Each round multiplies words 0 and 2 by the round
+    multipliers into 64-bit products, and the new words are
+    (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0));
+    the key is then advanced by the two increments.  Returns four uint32 arrays."""
+    c = [np.asarray(x, dtype=np.uint64) & 0xFFFFFFFF for x in counter]
+    k0, k1 = int(key[0]) & 0xFFFFFFFF, int(key[1]) & 0xFFFFFFFF
+    mask = np.uint64(0xFFFFFFFF)
+    for _ in range(10):
+        p0 = np.uint64(_PHILOX_M0) * c[0]
+        p1 = np.uint64(_PHILOX_M1) * c[2]
+        c = [(p1 >> np.uint64(32)) ^ c[1] ^ np.uint64(k0), p1 & mask,
+             (p0 >> np.uint64(32)) ^ c[3] ^ np.uint64(k1), p0 & mask]
+        k0 = (k0 + _PHILOX_W0) & 0xFFFFFFFF
+        k1 = (k1 + _PHILOX_W1) & 0xFFFFFFFF
+    return [x.astype(np.uint32) for x in c]
+
+
+def dropout_keep(nq, nk, bh, p, seed, offset):
+    """Keep mask Z [nq, nk] (bool) of head bh for query rows 0..nq-1 and keys
+    0..nk-1, as described above."""
+    i = np.arange(nq, dtype=np.uint64)[:, None]
+    j = np.arange(nk, dtype=np.uint64)[None, :]
+    words = philox4x32_10((j >> np.uint64(2), i, np.uint64(bh), np.uint64(offset & 0xFFFFFFFF)),
+                          (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))
+    sel = (j & np.uint64(3)).astype(np.int64)
+    w = np.choose(np.broadcast_to(sel, (nq, nk)), [np.broadcast_to(x, (nq, nk)) for x in words])
+    return w.astype(np.float64) / 2.0**32 >= p
+
+
+def forward_head_dropout(q, k, v, scale, causal, p, keep):
+    """(O, L) with dropout on the attention weights: O = (P o Z) V / (1 - p)."""
+    s = score_matrix(q, k, scale, causal)
+    P, L, _, _ = _softmax_rows(s)
+    return (P * keep / (1.0 - p)) @ _f64(v), L
+
+
+def backward_head_dropout(q, k, v, do, scale, causal, p, keep):
+    """Gradients with dropout.  With M = Z / (1 - p) and P~ = P o M:
+    dV = P~^T dO, dP = (dO V^T) o M, D_i = sum_j P_ij dP_ij (= dO_i . O_i),
+    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    s = score_matrix(q, k, scale, causal)
+    P, _, _, _ = _softmax_rows(s)
+    M = keep / (1.0 - p)
+    dV = (P * M).T @ do
+    dP = (do @ v.T) * M
+    D = (P * dP).sum(axis=1)
+    dS = P * (dP - D[:, None])
+    return scale * (dS @ k), scale * (dS.T @ q), dV, D
+
+
+def forward_dropout(q, k, v, scale, causal, p, seed, offset):
+    """Dense [B, H, N, D] forward with dropout."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, _ = q.shape
+    O = np.zeros((B, H, N, v.shape[-1]))
+    L = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            keep = dropout_keep(N, N, b * H + h, p, seed, offset)
+            O[b, h], L[b, h] = forward_head_dropout(q[b, h], k[b, h], v[b, h], scale, causal, p, keep)
+    return O, L
+
+
+def backward_dropout(q, k, v, do, scale, causal, p, seed, offset):
+    """Dense [B, H, N, D] backward with dropout: (dQ, dK, dV, D)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, _ = q.shape
+    dQ, dK, dV = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    Dv = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            keep = dropout_keep(N, N, b * H + h, p, seed, offset)
+            dQ[b, h], dK[b, h], dV[b, h], Dv[b, h] = backward_head_dropout(
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, p, keep)
     return dQ, dK, dV, Dv
 
 

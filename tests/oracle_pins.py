@@ -260,6 +260,70 @@ def check_cached_decoding(impl):
             np.testing.assert_allclose(Lb[b, h], Lh, atol=0)
 
 
+def check_philox_known_answers(impl):
+    """Philox4x32-10 against the known-answer vectors published with the
+    algorithm (counter, key) -> output."""
+    vectors = [
+        ((0, 0, 0, 0), (0, 0), (0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8)),
+        ((0xffffffff,) * 4, (0xffffffff,) * 2, (0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd)),
+        ((0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344), (0xa4093822, 0x299f31d0),
+         (0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1)),
+    ]
+    for ctr, key, want in vectors:
+        got = impl.philox4x32_10(ctr, key)
+        assert tuple(int(x) for x in got) == want
+
+
+def check_dropout(impl):
+    """Dropout: the keep fraction is binomial around 1 - p; p = 0 reduces to the
+    plain functions; forward and gradients against torch autograd of the same
+    masked computation (float64); finite differences; D_i = rowsum(dO o O)."""
+    import torch
+    keep = impl.dropout_keep(64, 256, 3, 0.3, 1234567, 5)
+    frac = keep.mean()
+    assert abs(frac - 0.7) < 4 * math.sqrt(0.7 * 0.3 / keep.size)
+    assert not np.array_equal(keep, impl.dropout_keep(64, 256, 4, 0.3, 1234567, 5))   # depends on the head
+    assert not np.array_equal(keep, impl.dropout_keep(64, 256, 3, 0.3, 1234568, 5))   # and on the seed
+    np.testing.assert_array_equal(impl.dropout_keep(5, 9, 3, 0.3, 1234567, 5), keep[:5, :9])
+    r = _rng(20)
+    n, d = 9, 4
+    q, k, v, do = r.standard_normal((4, n, d))
+    for causal in (False, True):
+        kp = impl.dropout_keep(n, n, 1, 0.0, 99, 0)
+        O0, L0 = impl.forward_head_dropout(q, k, v, 0.5, causal, 0.0, kp)
+        O1, L1 = impl.forward_head(q, k, v, 0.5, causal)
+        np.testing.assert_allclose(O0, O1, atol=1e-14)
+        g0 = impl.backward_head_dropout(q, k, v, do, 0.5, causal, 0.0, kp)
+        g1 = impl.backward_head(q, k, v, do, 0.5, causal)
+        for a, b in zip(g0, g1):
+            np.testing.assert_allclose(a, b, atol=1e-13)
+        p = 0.35
+        kp = impl.dropout_keep(n, n, 2, p, 4242, 7)
+        O, L = impl.forward_head_dropout(q, k, v, 0.5, causal, p, kp)
+        dQ, dK, dV, D = impl.backward_head_dropout(q, k, v, do, 0.5, causal, p, kp)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        s = 0.5 * tq @ tk.T
+        if causal:
+            s = s.masked_fill(torch.triu(torch.ones(n, n, dtype=torch.bool), 1), float("-inf"))
+        out = (torch.softmax(s, -1) * torch.tensor(kp / (1 - p))) @ tv
+        out.backward(torch.tensor(do))
+        np.testing.assert_allclose(O, out.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dQ, tq.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(dK, tk.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(dV, tv.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(D, (do * O).sum(1), atol=1e-13)
+        h = 1e-6
+        for which, grad in ((0, dQ), (1, dK), (2, dV)):
+            for (i, j) in ((0, 0), (4, 2), (8, 3)):
+                a_p = [q.copy(), k.copy(), v.copy()]
+                a_m = [q.copy(), k.copy(), v.copy()]
+                a_p[which][i, j] += h
+                a_m[which][i, j] -= h
+                fp = (impl.forward_head_dropout(*a_p, 0.5, causal, p, kp)[0] * do).sum()
+                fm = (impl.forward_head_dropout(*a_m, 0.5, causal, p, kp)[0] * do).sum()
+                assert abs((fp - fm) / (2 * h) - grad[i, j]) < 1e-6
+
+
 ALL_CHECKS = [
     check_split_tile_example,
     check_zero_query,
@@ -271,4 +335,6 @@ ALL_CHECKS = [
     check_finite_differences,
     check_gradient_invariants,
     check_cached_decoding,
+    check_philox_known_answers,
+    check_dropout,
 ]

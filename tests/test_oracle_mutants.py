@@ -47,8 +47,10 @@ MUTANTS = {
                          "    dK = scale * (dS.T @ k)\n    return dQ, dK, dV, D"),
     "dQ_missing_scale": ("    dQ = scale * (dS @ k)\n    dK",
                          "    dQ = (dS @ k)\n    dK"),
-    "D_missing_P": ("    D = (P * dP).sum(axis=1)\n    dS = P",
-                    "    D = dP.sum(axis=1)\n    dS = P"),
+    "D_missing_P": ("    D = (P * dP).sum(axis=1)\n    dS = P * (dP - D[:, None])\n    dQ = scale",
+                    "    D = dP.sum(axis=1)\n    dS = P * (dP - D[:, None])\n    dQ = scale"),
+    "dropout_D_missing_P": ("    D = (P * dP).sum(axis=1)\n    dS = P * (dP - D[:, None])\n    return scale",
+                            "    D = dP.sum(axis=1)\n    dS = P * (dP - D[:, None])\n    return scale"),
     "dV_missing_transpose": ("    dV = P.T @ do\n    dP = do @ v.T",
                              "    dV = P @ do\n    dP = do @ v.T"),
     "cached_mask_top_left": ("        s = np.where(j <= i + (nk - nq), s, -np.inf)",
@@ -59,6 +61,16 @@ MUTANTS = {
                          "        s = np.where(j <= i - (nk - nq), s, -np.inf)"),
     "cached_output_values_swapped": ("    return P @ _f64(v), L\n",
                                      "    return P @ _f64(k), L\n"),
+    "philox_words_swapped": ("        c = [(p1 >> np.uint64(32)) ^ c[1] ^ np.uint64(k0), p1 & mask,",
+                             "        c = [(p1 >> np.uint64(32)) ^ c[3] ^ np.uint64(k0), p1 & mask,"),
+    "philox_key_not_advanced": ("        k1 = (k1 + _PHILOX_W1) & 0xFFFFFFFF\n",
+                                "        k1 = k1\n"),
+    "dropout_keep_inverted": ("    return w.astype(np.float64) / 2.0**32 >= p\n",
+                              "    return w.astype(np.float64) / 2.0**32 < p\n"),
+    "dropout_no_rescale": ("    return (P * keep / (1.0 - p)) @ _f64(v), L\n",
+                           "    return (P * keep) @ _f64(v), L\n"),
+    "dropout_dP_unmasked": ("    dP = (do @ v.T) * M\n", "    dP = (do @ v.T)\n"),
+    "dropout_dV_unmasked": ("    dV = (P * M).T @ do\n", "    dV = P.T @ do\n"),
     "dP_transposed": ("    dV = P.T @ do\n    dP = do @ v.T",
                       "    dV = P.T @ do\n    dP = v @ do.T"),
 }
