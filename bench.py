@@ -224,6 +224,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="16-bit input type (the same synthetic draws, rounded to it)")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="attention dropout probability for the train workload (fa_fwd_dropout / fa_bwd_dropout)")
     ap.add_argument("--workload", choices=["train", "decode"], default="train",
                     help="train: causal fwd+bwd at B2 H32 N4096 D128 (the default); "
                          "decode: one cached decoding step, B16 H32, 1 query, 8192 keys, D128")
@@ -254,10 +256,11 @@ def main():
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_size(q), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    fwd_call, bwd_call = attention_calls(fa, args.dropout)
 
     def step():
-        fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+        fwd_call(q, k, v, o, lse, scale, stream)
+        bwd_call(q, k, v, o, lse, do, dq, dk, dv, scale, ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -278,10 +281,10 @@ def main():
         t_start.record(stream)
         for s in range(args.steps):
             ev[s][0].record(stream)
-            fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
+            fwd_call(q, k, v, o, lse, scale, stream)
             ev[s][1].record(stream)
             fa.fa_bwd_time_main_kernel(ev[s][3], ev[s][4])
-            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+            bwd_call(q, k, v, o, lse, do, dq, dk, dv, scale, ws, stream)
             ev[s][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -309,7 +312,7 @@ def main():
     src = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc",
                        "fa_tc_bwd128.cu" if path == "tcgen05" else "fa_simt.cu")
     # the ncu capture behind the table was of the bf16 run
-    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src)) if args.dtype == "bf16" else None
+    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src)) if args.dtype == "bf16" and args.dropout == 0 else None
     achieved = 2.5 * f_fwd / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": traffic, "kernel": dom_name,
@@ -317,11 +320,12 @@ def main():
                     "" if args.dtype == "bf16" else "; fp16 has the same nominal dense rate")}
 
     line = {
-        "metric": METRIC if args.dtype == "bf16" else METRIC.replace("bf16", args.dtype), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": (METRIC if args.dtype == "bf16" else METRIC.replace("bf16", args.dtype))
+                  + (f", attention dropout p={args.dropout:g}" if args.dropout > 0 else ""), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} causal", "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
-                   "kernel_path": path,
+                   "kernel_path": path, "dropout": args.dropout,
                    "l2": f"inputs {4 * q.numel() * 2 / 2**20:.0f} MiB > 129 MiB L2; no flush",
                    "parallelism": f"replicas x{world}"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
@@ -442,6 +446,19 @@ def bench_decode(fa, synth, args, dist, rank, world, local, device):
     print(json.dumps(line), flush=True)
 
 
+def attention_calls(fa, p_drop, seed=20251203):
+    """(forward, backward) enqueue functions of the timed step; with dropout the
+    same p, seed and offset in both."""
+    if p_drop > 0:
+        return (lambda q, k, v, o, lse, scale, st: fa.fa_fwd_dropout(q, k, v, o, lse, CAUSAL, p_drop, seed, 0, scale,
+                                                                     stream=st),
+                lambda q, k, v, o, lse, do, dq, dk, dv, scale, ws, st: fa.fa_bwd_dropout(
+                    q, k, v, o, lse, do, dq, dk, dv, CAUSAL, p_drop, seed, 0, scale, workspace=ws, stream=st))
+    return (lambda q, k, v, o, lse, scale, st: fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=st),
+            lambda q, k, v, o, lse, do, dq, dk, dv, scale, ws, st: fa.fa_bwd(
+                q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=st))
+
+
 def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, args):
     """Same metric through the public API with host buffers.  Every step copies
     its q, k, v, dO from pinned host memory, runs fa_fwd + fa_bwd and copies o,
@@ -468,6 +485,8 @@ def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, arg
     done = [ev() for _ in range(nbuf)]
     out_done = [ev() for _ in range(nbuf)]
 
+    fwd_call, bwd_call = attention_calls(fa, args.dropout)
+
     def run(steps, start_ev=None, end_ev=None):
         if start_ev is not None:
             start_ev.record(s_in)
@@ -485,8 +504,8 @@ def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, arg
                 stream.wait_event(out_done[b])  # step i-2's results have been downloaded
             q, k, v, do = din
             o, lse, dq, dk, dv = outs
-            fa.fa_fwd(q, k, v, o, lse, CAUSAL, scale, stream=stream)
-            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, workspace=ws, stream=stream)
+            fwd_call(q, k, v, o, lse, scale, stream)
+            bwd_call(q, k, v, o, lse, do, dq, dk, dv, scale, ws, stream)
             done[b].record(stream)
             s_out.wait_event(done[b])
             with torch.cuda.stream(s_out):

@@ -19,7 +19,7 @@ from ._lib import FA_BF16, FA_F16, FA_F32, FAError, lib, library_path  # noqa: F
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
            "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
-           "fa_decode", "fa_decode_workspace_size", "decode", "FAError"]
+           "fa_decode", "fa_decode_workspace_size", "decode", "fa_fwd_dropout", "fa_bwd_dropout", "FAError"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.float16: FA_F16}
 
@@ -149,6 +149,40 @@ def fa_bwd_static_ws(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_s
 
 
 STATIC_WS_BYTES = 16 << 20
+
+
+def fa_fwd_dropout(q, k, v, o, lse, causal, p_drop, seed, offset=0, scale=None, cu_seqlens=None, max_seqlen=None,
+                   stream=None):
+    """fa_fwd with attention dropout: weights dropped with probability p_drop
+    (decisions regenerated from seed and offset), kept ones scaled by
+    1 / (1 - p_drop); lse is that of the undropped softmax."""
+    _check(q, k, v, o, lse, cu_seqlens)
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    st = lib().fa_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, D, scale, int(bool(causal)),
+                              _ptr(cu_seqlens), T, _DT[q.dtype], float(p_drop), int(seed), int(offset),
+                              _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_fwd_dropout")
+
+
+def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, causal, p_drop, seed, offset=0, scale=None, cu_seqlens=None,
+                   max_seqlen=None, workspace=None, stream=None):
+    """fa_bwd for a forward run by fa_fwd_dropout with the same p_drop, seed, offset."""
+    _check(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens)
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    need = fa_bwd_workspace_size(q, cu_seqlens, max_seqlen)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                              B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T, _DT[q.dtype], float(p_drop),
+                              int(seed), int(offset), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_bwd_dropout")
 
 
 def fa_decode_workspace_size(q, k):

@@ -31,6 +31,10 @@ SIGNATURES = {
     "fa_launch_count": (_c.c_ulonglong, []),
     "fa_last_error_detail": (_c.c_char_p, []),
     "fa_bwd_time_main_kernel": (None, [_vp, _vp]),
+    "fa_fwd_dropout": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int, _vp, _int, _int, _f,
+                              _c.c_uint64, _c.c_uint32, _vp]),
+    "fa_bwd_dropout": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int,
+                              _vp, _int, _int, _f, _c.c_uint64, _c.c_uint32, _vp, _sz, _vp]),
     "fa_decode_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int]),
     "fa_decode": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _f, _int, _int, _vp, _sz, _vp]),
 }

@@ -75,6 +75,29 @@ fa_status check_tensor(const void* p) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Attention dropout arguments (nullptr: none).
+struct DropArgs {
+  float p;
+  uint64_t seed;
+  uint32_t offset;
+};
+
+// Keep iff the generator word w satisfies w / 2^32 >= p, i.e. w >= ceil(p 2^32)
+// (exact in double: p is a float and 2^32 a power of two).
+fa_status set_dropout(Problem& pr, fa_dtype dt, int D, const DropArgs* d) {
+  pr.dropout = 0;
+  if (d == nullptr) return FA_OK;
+  if (!(d->p >= 0.f && d->p < 1.f)) return FA_ERR_INVALID;
+  if (d->p == 0.f) return FA_OK;
+  if (!use_tensor_cores(dt, D)) return FA_ERR_UNSUPPORTED;  // the fp32 kernels have no dropout
+  pr.dropout = 1;
+  pr.drop_thr = (uint32_t)ceil((double)d->p * 4294967296.0);
+  pr.drop_scale = 1.0f / (1.0f - d->p);
+  pr.drop_seed = d->seed;
+  pr.drop_offset = d->offset;
+  return FA_OK;
+}
+
 }  // namespace
 
 void note_launches(unsigned n) { g_launches.fetch_add(n); }
@@ -179,8 +202,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int D, const int32_t* cu, int 
   return bytes;
 }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
-                 float scale, int causal, const int32_t* cu, int T, fa_dtype dt, void* stream) {
+static fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int D, float scale, int causal, const int32_t* cu, int T, fa_dtype dt, const DropArgs* drop,
+                          void* stream) {
   fa_status st = validate(B, H, N, D, scale, causal, cu, T, dt);
   if (st != FA_OK) return st;
   if (no_work(B, H, N, cu, T)) return FA_OK;
@@ -195,6 +219,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
   p.f16 = dt == FA_F16;
   p.scale = scale; p.causal = causal; p.cu = cu;
+  if ((st = set_dropout(p, dt, D, drop)) != FA_OK) return st;
   p.wait_limit_ns = g_wait_limit_ns.load();
   g_detail[0] = 0;
   if (note_error("status word", status_word(&p.status)) != cudaSuccess) return FA_ERR_CUDA;
@@ -203,9 +228,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-                 void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal,
-                 const int32_t* cu, int T, fa_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale,
+                          int causal, const int32_t* cu, int T, fa_dtype dt, const DropArgs* drop, void* workspace,
+                          size_t workspace_bytes, void* stream) {
   fa_status st = validate(B, H, N, D, scale, causal, cu, T, dt);
   if (st != FA_OK) return st;
   if (no_work(B, H, N, cu, T)) return FA_OK;
@@ -223,6 +249,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   p.B = B; p.H = H; p.N = N; p.D = D; p.T = cu ? T : 0;
   p.f16 = dt == FA_F16;
   p.scale = scale; p.causal = causal; p.cu = cu;
+  if ((st = set_dropout(p, dt, D, drop)) != FA_OK) return st;
   p.wait_limit_ns = g_wait_limit_ns.load();
   const long long rows = p.rows();
   p.dvec = static_cast<float*>(workspace);
@@ -241,6 +268,34 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (e == cudaSuccess && ev_stop) e = note_error("timing event", cudaEventRecord(ev_stop, s));
   if (e == cudaSuccess && tc) e = launch_dq_convert(p, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                 float scale, int causal, const int32_t* cu, int T, fa_dtype dt, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, D, scale, causal, cu, T, dt, nullptr, stream);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal,
+                 const int32_t* cu, int T, fa_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D, scale, causal, cu, T, dt, nullptr, workspace,
+                  workspace_bytes, stream);
+}
+
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                         int D, float scale, int causal, const int32_t* cu, int T, fa_dtype dt, float p_drop,
+                         uint64_t seed, uint32_t offset, void* stream) {
+  const DropArgs d{p_drop, seed, offset};
+  return fwd_impl(q, k, v, o, lse, B, H, N, D, scale, causal, cu, T, dt, &d, stream);
+}
+
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale,
+                         int causal, const int32_t* cu, int T, fa_dtype dt, float p_drop, uint64_t seed,
+                         uint32_t offset, void* workspace, size_t workspace_bytes, void* stream) {
+  const DropArgs d{p_drop, seed, offset};
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D, scale, causal, cu, T, dt, &d, workspace,
+                  workspace_bytes, stream);
 }
 
 size_t fa_decode_workspace_size(int B, int H, int nq, int nk, int D, fa_dtype dt) {

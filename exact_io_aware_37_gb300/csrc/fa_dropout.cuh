@@ -1,0 +1,89 @@
+// Attention dropout decisions, regenerated wherever they are needed
+// (tensortonic.com "FlashAttention" section 7: the backward pass must
+// reproduce the forward pass's dropout decisions from saved random-number-
+// generator information instead of sampling a new mask).
+//
+// The generator is Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011), a counter-based generator: the
+// decision for element (i, j) of head bh = b * H + h is word j mod 4 of
+// Philox4x32-10 applied to counter (j / 4, i, bh, offset) under key
+// (seed mod 2^32, seed / 2^32), and the element is kept iff that word is at
+// least thr = ceil(p * 2^32) (i.e. word / 2^32 >= p).  Kept weights are
+// multiplied by 1 / (1 - p).  i and j count from the start of the element's
+// own sequence.
+#pragma once
+
+#include <stdint.h>
+
+#include "fa_internal.cuh"
+
+namespace fa {
+
+struct DropParams {
+  uint32_t thr;      // keep iff word >= thr
+  float scale;       // 1 / (1 - p)
+  uint32_t seed_lo, seed_hi, offset;
+};
+
+// Ten rounds; each multiplies words 0 and 2 by the round multipliers into
+// 64-bit products and forms (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+// lo(M0 c0)); the key advances by the Weyl increments after every round.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Keep bits (bit t for key j0 + t) of keys j0 .. j0 + 3 (j0 a multiple of 4)
+// for query row i: one generator call.
+__device__ __forceinline__ uint32_t keep4(const DropParams& d, uint32_t i, uint32_t j0, uint32_t bh) {
+  const uint4 w = philox4x32_10(make_uint4(j0 >> 2, i, bh, d.offset), d.seed_lo, d.seed_hi);
+  return (w.x >= d.thr ? 1u : 0u) | (w.y >= d.thr ? 2u : 0u) | (w.z >= d.thr ? 4u : 0u) | (w.w >= d.thr ? 8u : 0u);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& w, uint32_t t) {
+  return t == 0 ? w.x : t == 1 ? w.y : t == 2 ? w.z : w.w;
+}
+
+// Keep bits (bit c for query q0 + c, c < 64) of this thread's key `key` when
+// keys sit on the lanes of a warp and lanes 4m .. 4m+3 hold keys 4m' .. 4m'+3
+// (key = 4 * (key / 4) + lane % 4).  The four lanes sharing key / 4 need the
+// four words of the same generator call for each query, so each of them
+// computes the calls for a quarter of the queries (q = q0 + 4g + lane % 4)
+// and the words are exchanged within the quad: in round r lane t receives,
+// from lane (t + r) mod 4, that lane's word t.  All 32 lanes must call this.
+__device__ __forceinline__ uint64_t keep64_keys_on_lanes(const DropParams& d, uint32_t key, uint32_t q0,
+                                                         uint32_t bh, int lane) {
+  const uint32_t t = lane & 3;
+  const uint32_t quad_base = lane & ~3;
+  uint64_t bits = 0;
+#pragma unroll 4
+  for (int g = 0; g < 16; ++g) {
+    const uint4 w = philox4x32_10(make_uint4(key >> 2, q0 + 4 * g + t, bh, d.offset), d.seed_lo, d.seed_hi);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t send = word_of(w, (t - r) & 3);  // this lane's word for lane (t - r) mod 4
+      const uint32_t got = __shfl_sync(0xffffffffu, send, quad_base | ((t + r) & 3));
+      if (got >= d.thr) bits |= 1ull << (4 * g + ((t + r) & 3));
+    }
+  }
+  return bits;
+}
+
+inline DropParams drop_params_of(const Problem& p) {
+  DropParams d;
+  d.thr = p.drop_thr;
+  d.scale = p.drop_scale;
+  d.seed_lo = (uint32_t)(p.drop_seed & 0xffffffffu);
+  d.seed_hi = (uint32_t)(p.drop_seed >> 32);
+  d.offset = p.drop_offset;
+  return d;
+}
+
+}  // namespace fa

@@ -40,6 +40,11 @@ struct Problem {
   int B, H, N, D;
   int T;            // packed token count (0 when dense)
   int f16;          // 16-bit tensors: 1 = fp16, 0 = bf16
+  int dropout;      // attention dropout on (the tensor-core kernels only)
+  uint32_t drop_thr;    // keep iff generator word >= drop_thr
+  float drop_scale;     // 1 / (1 - p)
+  uint64_t drop_seed;
+  uint32_t drop_offset;
   float scale;
   int causal;
   const int32_t* cu;  // device pointer or nullptr

@@ -33,6 +33,7 @@
 // theirs (setmaxnreg).
 #include <math.h>
 
+#include "fa_dropout.cuh"
 #include "fa_internal.cuh"
 #include "fa_tmap.cuh"
 #include "ptx.cuh"
@@ -50,6 +51,7 @@ constexpr int kMmaWarp = 9;
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo;
+  DropParams drop;  // used by the dropout instantiation only
   const float* lse;
   const float* dvec;
   float* dq_acc;
@@ -93,7 +95,7 @@ struct BwdCfg {
   static_assert(kSmemBytes <= 232448, "backward tiles exceed the shared-memory limit");
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -189,6 +191,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       const int st = k & 1;
       const float* sl = s_l + st * 128 + ch * 64;
       const float* sd = s_d + st * 128 + ch * 64;
+      // dropout decisions of (this half's 64 queries, this key), regenerated
+      uint64_t keepm = ~0ull;
+      if constexpr (kDrop)
+        keepm = keep64_keys_on_lanes(p.drop, (uint32_t)key, (uint32_t)(qi * kBM + ch * 64), (uint32_t)(b * p.H + h),
+                                     lane);
       // L / D of this query tile are visible once bar_qf completes; S^T once bar_s does
       if (!warp_wait(bar_qf + st, (k >> 1) & 1, w) || !warp_wait(bar_s, k & 1, w)) {
         ok = false;
@@ -217,7 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // P^T as bf16 pairs into this half's first 32 score columns (already read)
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) {
+          if constexpr (kDrop)  // dV takes the dropped weights, scaled by 1 / (1 - p)
+            pk[c] = pack16x2<F16>((keepm >> (2 * c)) & 1 ? pr[2 * c] * p.drop.scale : 0.f,
+                                  (keepm >> (2 * c + 1)) & 1 ? pr[2 * c + 1] * p.drop.scale : 0.f);
+          else
+            pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
+        }
         tmem_st32(t_s, pk);
         tmem_st_wait();
       }
@@ -240,8 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c8 * 8 + 2 * e;
-          const float d0 = pr[c] * (__uint_as_float(sv[c >> 5][c & 31]) - sd[c]);
-          const float d1 = pr[c + 1] * (__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - sd[c + 1]);
+          float dp0 = __uint_as_float(sv[c >> 5][c & 31]), dp1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
+          if constexpr (kDrop) {  // dP of the dropped weights: masked and scaled like them
+            dp0 = (keepm >> c) & 1 ? dp0 * p.drop.scale : 0.f;
+            dp1 = (keepm >> (c + 1)) & 1 ? dp1 * p.drop.scale : 0.f;
+          }
+          const float d0 = pr[c] * (dp0 - sd[c]);
+          const float d1 = pr[c + 1] * (dp1 - sd[c + 1]);
           u[e] = pack16x2<F16>(d0, d1);
         }
         // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
@@ -498,7 +516,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
   }
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   using C = BwdCfg<D>;
   BwdParams bp;
@@ -520,10 +538,11 @@ cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   bp.c2 = p.scale * kLog2e;
   bp.scale = p.scale;
   bp.causal = p.causal;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  bp.drop = drop_params_of(p);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, F16, kDrop>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kBN - 1) / kBN, p.H, p.B);
-  tc_bwd_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
+  tc_bwd_kernel<D, F16, kDrop><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }
@@ -547,7 +566,10 @@ cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s) {
 
 
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s) {
-  if (p.D == 64) return p.f16 ? launch_bwd_d<64, true>(p, s) : launch_bwd_d<64, false>(p, s);
+  if (p.D == 64) {
+    if (p.dropout) return p.f16 ? launch_bwd_d<64, true, true>(p, s) : launch_bwd_d<64, false, true>(p, s);
+    return p.f16 ? launch_bwd_d<64, true, false>(p, s) : launch_bwd_d<64, false, false>(p, s);
+  }
   if (p.D == 128) return launch_tc_bwd128(p, s);
   return cudaErrorInvalidValue;
 }

@@ -36,6 +36,7 @@
 // warpgroups and 136 for the producer / MMA warpgroup (setmaxnreg).
 #include <math.h>
 
+#include "fa_dropout.cuh"
 #include "fa_internal.cuh"
 #include "fa_tmap.cuh"
 #include "ptx.cuh"
@@ -62,6 +63,7 @@ static_assert(2 * 128 * kBwdComputeRegs + 128 * kBwdSupportRegs <= kThreads * kL
 
 struct Bwd128Params {
   CUtensorMap tq, tk, tv, tdo;
+  DropParams drop;  // used by the dropout instantiation only
   const float* lse;
   const float* dvec;
   float* dq_acc;
@@ -93,7 +95,7 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
 
-template <bool F16>
+template <bool F16, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_constant__ Bwd128Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,6 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       const int st = k & 1;
       const float4* sl4 = reinterpret_cast<const float4*>(s_l + st * 128 + ch * 64);
       const float4* sd4 = reinterpret_cast<const float4*>(s_d + st * 128 + ch * 64);
+      // dropout decisions of (this half's 64 queries, this key), regenerated
+      uint64_t keepm = ~0ull;
+      if constexpr (kDrop)
+        keepm = keep64_keys_on_lanes(p.drop, (uint32_t)key, (uint32_t)(qi * kTile + ch * 64), (uint32_t)(b * p.H + h),
+                                     lane);
       ok = ok && warp_wait(bar_qf + st, (k >> 1) & 1, w) && warp_wait(bar_s, k & 1, w);
       tc_fence_after();
       uint32_t sv[2][32];
@@ -245,7 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) {
+          if constexpr (kDrop)  // dV takes the dropped weights, scaled by 1 / (1 - p)
+            pk[c] = pack16x2<F16>((keepm >> (2 * c)) & 1 ? pr[2 * c] * p.drop.scale : 0.f,
+                                  (keepm >> (2 * c + 1)) & 1 ? pr[2 * c + 1] * p.drop.scale : 0.f);
+          else
+            pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
+        }
         tmem_st32(t_s, pk);
         tmem_st_wait();
       }
@@ -270,8 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         for (int e = 0; e < 4; ++e) {
           const int c = c8 * 8 + 2 * e;
           float t0, t1, d0, d1;  // dS = P o (dP - D), two columns per packed op
-          fsub2(t0, t1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
-                dv[2 * e], dv[2 * e + 1]);
+          float dp0 = __uint_as_float(sv[c >> 5][c & 31]), dp1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
+          if constexpr (kDrop) {  // dP of the dropped weights: masked and scaled like them
+            dp0 = (keepm >> c) & 1 ? dp0 * p.drop.scale : 0.f;
+            dp1 = (keepm >> (c + 1)) & 1 ? dp1 * p.drop.scale : 0.f;
+          }
+          fsub2(t0, t1, dp0, dp1, dv[2 * e], dv[2 * e + 1]);
           fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
           dsp[4 * c8 + e] = pack16x2<F16>(d0, d1);
         }
@@ -509,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 
 }  // namespace
 
-template <bool F16>
+template <bool F16, bool kDrop>
 cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   Bwd128Params bp;
   if (!make_map16(&bp.tq, p.q, p, kTile) || !make_map16(&bp.tk, p.k, p, kTile) ||
@@ -530,16 +547,18 @@ cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   bp.c2 = p.scale * kLog2e;
   bp.scale = p.scale;
   bp.causal = p.causal;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  bp.drop = drop_params_of(p);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16, kDrop>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kTile - 1) / kTile, p.H, p.B);
-  tc_bwd128_kernel<F16><<<grid, kThreads, kSmemBytes, s>>>(bp);
+  tc_bwd128_kernel<F16, kDrop><<<grid, kThreads, kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }
 
 cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
-  return p.f16 ? launch_bwd128_t<true>(p, s) : launch_bwd128_t<false>(p, s);
+  if (p.dropout) return p.f16 ? launch_bwd128_t<true, true>(p, s) : launch_bwd128_t<false, true>(p, s);
+  return p.f16 ? launch_bwd128_t<true, false>(p, s) : launch_bwd128_t<false, false>(p, s);
 }
 
 }  // namespace fa

@@ -35,6 +35,7 @@
 // O_1 [384,384+D); P_t (bf16 pairs) overwrites S_t columns [0,64).
 #include <math.h>
 
+#include "fa_dropout.cuh"
 #include "fa_internal.cuh"
 #include "fa_tmap.cuh"
 #include "ptx.cuh"
@@ -54,6 +55,7 @@ constexpr int kFwdHeadGroup = 16;  // heads per group of the causal block order 
 
 struct FwdParams {
   CUtensorMap tq, tk, tv;
+  DropParams drop;  // used by the dropout instantiation only
   __nv_bfloat16* o;  // 16-bit storage: bf16 or fp16 per F16
   float* lse;
   const int32_t* cu;
@@ -80,7 +82,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
         // p = 2^(s * scale * log2(e) - m_ref), two columns per packed FMA
         float rs0 = 0.f, rs1 = 0.f;
+        uint32_t kbits = 0;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[32];
@@ -217,8 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                   p.c2, nmu, nmu);
             const float p0 = ex2_approx(a0);
             const float p1 = ex2_approx(a1);
-            fadd2(rs0, rs1, p0, p1);
-            pk[c] = pack16x2<F16>(p0, p1);
+            fadd2(rs0, rs1, p0, p1);  // the normaliser is that of the undropped weights
+            if constexpr (kDrop) {
+              // dropped weights enter PV scaled by 1 / (1 - p); one generator call per 4 keys
+              if ((c & 1) == 0) kbits = keep4(p.drop, (uint32_t)i, (uint32_t)(k0 + e0), (uint32_t)(b * p.H + h));
+              const uint32_t sh = (c & 1) * 2;
+              pk[c] = pack16x2<F16>((kbits >> sh) & 1u ? p0 * p.drop.scale : 0.f,
+                                    (kbits >> (sh + 1)) & 1u ? p1 * p.drop.scale : 0.f);
+            } else {
+              pk[c] = pack16x2<F16>(p0, p1);
+            }
           }
           tmem_st32(t_s + 32 * hf, pk);
         }
@@ -417,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool kDrop>
 cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   using C = FwdCfg<D>;
   FwdParams fp;
@@ -435,11 +446,12 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   fp.T = p.T;
   fp.c2 = p.scale * kLog2e;
   fp.causal = p.causal;
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  fp.drop = drop_params_of(p);
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, F16, kDrop>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("forward smem attribute", e);
   const int n_qt = (p.N + kBM - 1) / kBM;
   dim3 grid((n_qt + 1) / 2, p.H, p.B);
-  tc_fwd_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
+  tc_fwd_kernel<D, F16, kDrop><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
   note_launches(1);
   return note_error("forward launch", cudaGetLastError());
 }
@@ -447,8 +459,13 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s) {
-  if (p.D == 64) return p.f16 ? launch_fwd_d<64, true>(p, s) : launch_fwd_d<64, false>(p, s);
-  if (p.D == 128) return p.f16 ? launch_fwd_d<128, true>(p, s) : launch_fwd_d<128, false>(p, s);
+  if (p.dropout) {
+    if (p.D == 64) return p.f16 ? launch_fwd_d<64, true, true>(p, s) : launch_fwd_d<64, false, true>(p, s);
+    if (p.D == 128) return p.f16 ? launch_fwd_d<128, true, true>(p, s) : launch_fwd_d<128, false, true>(p, s);
+  } else {
+    if (p.D == 64) return p.f16 ? launch_fwd_d<64, true, false>(p, s) : launch_fwd_d<64, false, false>(p, s);
+    if (p.D == 128) return p.f16 ? launch_fwd_d<128, true, false>(p, s) : launch_fwd_d<128, false, false>(p, s);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -220,6 +220,30 @@ void fa_bwd_time_main_kernel(void* start_event, void* stop_event);
  */
 unsigned long long fa_launch_count(void);
 
+/* Attention dropout (tensortonic.com "FlashAttention" section 7: the backward
+ * must reproduce the forward's dropout decisions from saved generator state).
+ * Same arguments as fa_fwd / fa_bwd plus:
+ *   p_drop  probability of dropping an attention weight, 0 <= p_drop < 1
+ *           (FA_ERR_INVALID otherwise; 0 gives exactly fa_fwd / fa_bwd);
+ *   seed, offset  select the decisions, which are regenerated, never stored:
+ *           element (i, j) of head bh = b * H + h (i, j counted from the start
+ *           of the element's own sequence) is kept iff word j mod 4 of the
+ *           counter-based generator Philox4x32-10 (Salmon et al., SC 2011) on
+ *           counter (j / 4, i, bh, offset) and key (seed mod 2^32, seed / 2^32),
+ *           divided by 2^32, is >= p_drop.
+ * Kept weights are scaled by 1 / (1 - p_drop): O = (P o Z) V / (1 - p_drop); lse
+ * is that of the undropped softmax.  fa_bwd_dropout must get the same
+ * p_drop, seed and offset as the forward that produced o.  Tensor-core path
+ * only (bf16 / fp16, D 64 or 128): FA_ERR_UNSUPPORTED for float32 with
+ * p_drop > 0. */
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                         int D, float scale, int causal, const int32_t* cu_seqlens, int total_tokens,
+                         fa_dtype dtype, float p_drop, uint64_t seed, uint32_t offset, void* stream);
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale,
+                         int causal, const int32_t* cu_seqlens, int total_tokens, fa_dtype dtype, float p_drop,
+                         uint64_t seed, uint32_t offset, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Cached decoding step (tensortonic.com "FlashAttention" section 8: a
  * generation step has a few new queries and a long set of cached keys and
  * values; section 9: the newest query must be aligned with its actual position

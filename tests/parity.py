@@ -76,9 +76,11 @@ def rel_frob(a, b):
     return np.linalg.norm(a - b) / (den if den > 0 else 1.0)
 
 
-def compare(dtype, got, ref, what, grads=True):
-    """got/ref: dicts with o, lse (and dq, dk, dv) as float64 arrays."""
-    tol = TOL[dtype]
+def compare(dtype, got, ref, what, grads=True, o_scale=1.0):
+    """got/ref: dicts with o, lse (and dq, dk, dv) as float64 arrays.  o_scale
+    widens the O bound (dropout magnifies the weights by 1 / (1 - p))."""
+    tol = dict(TOL[dtype])
+    tol["o_max"] *= o_scale
     assert np.isfinite(got["o"]).all(), f"{what}: O has NaN/Inf (unwritten rows?)"
     e_o = np.abs(got["o"] - ref["o"]).max() if got["o"].size else 0.0
     assert e_o <= tol["o_max"], f"{what}: max|dO| = {e_o:.3e}"

@@ -117,6 +117,23 @@ def test_strerror_and_path_names(lib):
     assert lib.fa_path_name(2, 32) is None
 
 
+def test_dropout_validation(lib):
+    def fwd(p, dt=0, **kw):
+        a = dict(q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=1, N=128, D=128, scale=0.1, causal=1,
+                 cu=None, T=0)
+        a.update(kw)
+        return lib.fa_fwd_dropout(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                                  a["scale"], a["causal"], a["cu"], a["T"], dt, p, 7, 0, None)
+    assert fwd(-0.1) == INVALID
+    assert fwd(1.0) == INVALID
+    assert fwd(float("nan")) == INVALID
+    assert fwd(0.2, dt=1, D=64) == UNSUPPORTED   # no dropout on the float32 path
+    assert fwd(0.2, B=0) == OK
+    bwd = lib.fa_bwd_dropout(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 128, 128,
+                             0.1, 1, None, 0, 0, 1.5, 7, 0, 0x100000, 1 << 30, None)
+    assert bwd == INVALID
+
+
 def test_decode_validation_and_workspace(lib):
     def dec(ws=0x100000, ws_bytes=1 << 30, **kw):
         a = dict(q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=2, nq=1, nk=1000, D=128, scale=0.1,
