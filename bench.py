@@ -226,6 +226,8 @@ def main():
                     help="16-bit input type (the same synthetic draws, rounded to it)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="attention dropout probability for the train workload (fa_fwd_dropout / fa_bwd_dropout)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="train workload with fa_bwd_deterministic (dQ without atomics)")
     ap.add_argument("--workload", choices=["train", "decode"], default="train",
                     help="train: causal fwd+bwd at B2 H32 N4096 D128 (the default); "
                          "decode: one cached decoding step, B16 H32, 1 query, 8192 keys, D128")
@@ -256,7 +258,7 @@ def main():
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_size(q), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    fwd_call, bwd_call = attention_calls(fa, args.dropout)
+    fwd_call, bwd_call = attention_calls(fa, args.dropout, deterministic=args.deterministic)
 
     def step():
         fwd_call(q, k, v, o, lse, scale, stream)
@@ -309,10 +311,13 @@ def main():
     # by events the library records right around it
     dom_ms = statistics.mean(main_ms)
     dom_name = "tc_bwd128_kernel" if path == "tcgen05" else "simt backward kernels"
+    if args.deterministic:
+        dom_name = "tc_bwd_kernel (dK, dV) + tc_bwd_dq_kernel (dQ)"
     src = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc",
                        "fa_tc_bwd128.cu" if path == "tcgen05" else "fa_simt.cu")
     # the ncu capture behind the table was of the bf16 run
-    traffic = TRAFFIC_BY_SOURCE.get(kernel_source_sha(src)) if args.dtype == "bf16" and args.dropout == 0 else None
+    traffic = (TRAFFIC_BY_SOURCE.get(kernel_source_sha(src))
+               if args.dtype == "bf16" and args.dropout == 0 and not args.deterministic else None)
     achieved = 2.5 * f_fwd / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": achieved / peak_tf, "traffic": traffic, "kernel": dom_name,
@@ -321,11 +326,12 @@ def main():
 
     line = {
         "metric": (METRIC if args.dtype == "bf16" else METRIC.replace("bf16", args.dtype))
-                  + (f", attention dropout p={args.dropout:g}" if args.dropout > 0 else ""), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                  + (f", attention dropout p={args.dropout:g}" if args.dropout > 0 else "")
+                  + (", deterministic backward" if args.deterministic else ""), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
         "config": {"workload": f"{WORKLOAD} causal", "B": B, "H": H, "N": N, "D": D, "causal": CAUSAL,
-                   "kernel_path": path, "dropout": args.dropout,
+                   "kernel_path": path, "dropout": args.dropout, "deterministic_bwd": args.deterministic,
                    "l2": f"inputs {4 * q.numel() * 2 / 2**20:.0f} MiB > 129 MiB L2; no flush",
                    "parallelism": f"replicas x{world}"},
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
@@ -446,9 +452,15 @@ def bench_decode(fa, synth, args, dist, rank, world, local, device):
     print(json.dumps(line), flush=True)
 
 
-def attention_calls(fa, p_drop, seed=20251203):
+def attention_calls(fa, p_drop, seed=20251203, deterministic=False):
     """(forward, backward) enqueue functions of the timed step; with dropout the
     same p, seed and offset in both."""
+    if deterministic:
+        fwd = (lambda q, k, v, o, lse, scale, st: fa.fa_fwd_dropout(q, k, v, o, lse, CAUSAL, p_drop, seed, 0, scale,
+                                                                    stream=st))
+        return (fwd, lambda q, k, v, o, lse, do, dq, dk, dv, scale, ws, st: fa.fa_bwd_deterministic(
+            q, k, v, o, lse, do, dq, dk, dv, CAUSAL, scale, p_drop=p_drop, seed=seed, offset=0, workspace=ws,
+            stream=st))
     if p_drop > 0:
         return (lambda q, k, v, o, lse, scale, st: fa.fa_fwd_dropout(q, k, v, o, lse, CAUSAL, p_drop, seed, 0, scale,
                                                                      stream=st),
@@ -485,7 +497,7 @@ def e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, arg
     done = [ev() for _ in range(nbuf)]
     out_done = [ev() for _ in range(nbuf)]
 
-    fwd_call, bwd_call = attention_calls(fa, args.dropout)
+    fwd_call, bwd_call = attention_calls(fa, args.dropout, deterministic=args.deterministic)
 
     def run(steps, start_ev=None, end_ev=None):
         if start_ev is not None:

@@ -19,7 +19,8 @@ from ._lib import FA_BF16, FA_F16, FA_F32, FAError, lib, library_path  # noqa: F
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
            "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
-           "fa_decode", "fa_decode_workspace_size", "decode", "fa_fwd_dropout", "fa_bwd_dropout", "FAError"]
+           "fa_decode", "fa_decode_workspace_size", "decode", "fa_fwd_dropout", "fa_bwd_dropout",
+           "fa_bwd_deterministic", "FAError"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.float16: FA_F16}
 
@@ -183,6 +184,24 @@ def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, causal, p_drop, seed, offs
                               _stream(stream))
     if st != 0:
         raise FAError(st, "fa_bwd_dropout")
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_seqlens=None, max_seqlen=None,
+                         p_drop=0.0, seed=0, offset=0, workspace=None, stream=None):
+    """fa_bwd (or fa_bwd_dropout) with every sum in a fixed order: repeated
+    calls give bit-identical gradients (dQ from a query-stationary kernel)."""
+    _check(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens)
+    B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if workspace is None:
+        rows = (H * T) if cu_seqlens is not None else (B * H * N)
+        workspace = torch.empty(max((rows * 4 + 255) // 256 * 256, 256), dtype=torch.uint8, device=q.device)
+    st = lib().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T,
+                                    _DT[q.dtype], float(p_drop), int(seed), int(offset), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_bwd_deterministic")
 
 
 def fa_decode_workspace_size(q, k):

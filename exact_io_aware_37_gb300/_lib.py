@@ -35,6 +35,8 @@ SIGNATURES = {
                               _c.c_uint64, _c.c_uint32, _vp]),
     "fa_bwd_dropout": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int,
                               _vp, _int, _int, _f, _c.c_uint64, _c.c_uint32, _vp, _sz, _vp]),
+    "fa_bwd_deterministic": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int,
+                                    _vp, _int, _int, _f, _c.c_uint64, _c.c_uint32, _vp, _sz, _vp]),
     "fa_decode_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int]),
     "fa_decode": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _f, _int, _int, _vp, _sz, _vp]),
 }

@@ -22,7 +22,7 @@ LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_tc_bwd128.cu", "fa_static_ws.cu",
-           "fa_decode.cu"]
+           "fa_decode.cu", "fa_tc_bwd_dq.cu"]
 
 # The tensor-core kernels move registers between warpgroups with setmaxnreg
 # (384-thread kernels: 200 + 200 + 104 per thread from 168 at launch; the
@@ -31,7 +31,7 @@ SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_tc_bwd
 # that ptxas compiled with fewer would wait forever in setmaxnreg.inc, so the
 # build refuses it.
 # kernel name -> registers per thread it must be compiled with (checked in order)
-SPLIT_KERNELS = {"tc_bwd128_kernel": 168, "tc_fwd_kernel": 168, "tc_bwd_kernel": 168}
+SPLIT_KERNELS = {"tc_bwd128_kernel": 168, "tc_fwd_kernel": 168, "tc_bwd_kernel": 168, "tc_bwd_dq_kernel": 168}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]

@@ -231,7 +231,7 @@ static fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, 
 static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
                           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale,
                           int causal, const int32_t* cu, int T, fa_dtype dt, const DropArgs* drop, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+                          size_t workspace_bytes, void* stream, bool deterministic = false) {
   fa_status st = validate(B, H, N, D, scale, causal, cu, T, dt);
   if (st != FA_OK) return st;
   if (no_work(B, H, N, cu, T)) return FA_OK;
@@ -240,7 +240,9 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
   if (lse == nullptr) return FA_ERR_INVALID;
   if (!aligned(lse, 4)) return FA_ERR_ALIGN;
   if (cu != nullptr && !aligned(cu, 4)) return FA_ERR_ALIGN;
-  const size_t need = fa_bwd_workspace_size(B, H, N, D, cu, T, dt);
+  // the deterministic path keeps no float32 dQ accumulator: only D_i
+  const size_t need = deterministic ? round_up((size_t)row_count(B, H, N, cu, T) * sizeof(float), 256)
+                                    : fa_bwd_workspace_size(B, H, N, D, cu, T, dt);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
 
   Problem p{};
@@ -253,7 +255,7 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
   p.wait_limit_ns = g_wait_limit_ns.load();
   const long long rows = p.rows();
   p.dvec = static_cast<float*>(workspace);
-  p.dq_acc = use_tensor_cores(dt, D)
+  p.dq_acc = use_tensor_cores(dt, D) && !deterministic
                  ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)rows * 4, 256))
                  : nullptr;
   g_detail[0] = 0;
@@ -264,6 +266,13 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
   const bool tc = kHaveTcBwd && use_tensor_cores(dt, D);
   cudaError_t e = launch_bwd_preprocess(p, dt, p.dq_acc != nullptr, s);
   if (e == cudaSuccess && ev_start) e = note_error("timing event", cudaEventRecord(ev_start, s));
+  if (e == cudaSuccess && tc && deterministic) {
+    // dK, dV key-stationary and dQ query-stationary: no atomics anywhere
+    e = launch_tc_bwd_dkdv(p, s);
+    if (e == cudaSuccess) e = launch_tc_bwd_dq(p, s);
+    if (e == cudaSuccess && ev_stop) e = note_error("timing event", cudaEventRecord(ev_stop, s));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
   if (e == cudaSuccess) e = tc ? launch_tc_bwd(p, s) : launch_simt_bwd(p, dt, s);
   if (e == cudaSuccess && ev_stop) e = note_error("timing event", cudaEventRecord(ev_stop, s));
   if (e == cudaSuccess && tc) e = launch_dq_convert(p, s);
@@ -296,6 +305,16 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
   const DropArgs d{p_drop, seed, offset};
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D, scale, causal, cu, T, dt, &d, workspace,
                   workspace_bytes, stream);
+}
+
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                               float scale, int causal, const int32_t* cu, int T, fa_dtype dt, float p_drop,
+                               uint64_t seed, uint32_t offset, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  const DropArgs d{p_drop, seed, offset};
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, D, scale, causal, cu, T, dt, &d, workspace,
+                  workspace_bytes, stream, true);
 }
 
 size_t fa_decode_workspace_size(int B, int H, int nq, int nk, int D, fa_dtype dt) {

@@ -125,6 +125,10 @@ cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s);
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s);  // main kernel only
 cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s);  // main kernel only, D = 128
 cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s);  // dQ = bf16(scale * dQ_acc)
+// Deterministic backward: dK / dV (key-stationary, no dQ product) and dQ
+// (query-stationary, accumulated in tensor memory, no atomics).
+cudaError_t launch_tc_bwd_dkdv(const Problem& p, cudaStream_t s);
+cudaError_t launch_tc_bwd_dq(const Problem& p, cudaStream_t s);
 
 // Cached decoding (fa_decode.cu).  Problem fields q, k, v, o, lse, B, H, D,
 // scale, causal are used; nq / nk are the query and cached-key counts.

@@ -95,7 +95,9 @@ struct BwdCfg {
   static_assert(kSmemBytes <= 232448, "backward tiles exceed the shared-memory limit");
 };
 
-template <int D, bool F16, bool kDrop>
+// kDq = false: dK and dV only (the deterministic backward takes dQ from the
+// query-stationary kernel in fa_tc_bwd_dq.cu).
+template <int D, bool F16, bool kDrop, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -270,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
 
+      if constexpr (!kDq) continue;
       // dQ of this query tile into the float32 accumulator
       if (!warp_wait(bar_dq, k & 1, w)) {
         ok = false;
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         issue_nn(128, kV, kDO + st * kStageDesc);
         mma_commit(bar_dp);
         // S^T = K Q^T into the columns the previous dQ used, once it is drained
-        if (k > 0) {
+        if (kDq && k > 0) {
           if (!mbar_wait(bar_dqfree, (k - 1) & 1, w)) break;
           tc_fence_after();
         }
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         mma_commit(bar_qe + st);
         // dQ over the 128 keys (K = 16 keys per MMA): the dS buffer read MN-major
         // (queries contiguous) and K read MN-major (head width contiguous)
-        {
+        if constexpr (kDq) {
           uint64_t a[8], b[8];
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -491,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             b[ks] = (C::kDqTransposed ? mDS : mK) + ((ks * 2048) >> 4);
           }
           mma_ss_x8(tmem + 0, a, b, id_dq, 0u);
+          mma_commit(bar_dq);
         }
-        mma_commit(bar_dq);
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(bar_done);
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
   }
 }
 
-template <int D, bool F16, bool kDrop>
+template <int D, bool F16, bool kDrop, bool kDq>
 cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   using C = BwdCfg<D>;
   BwdParams bp;
@@ -539,10 +542,10 @@ cudaError_t launch_bwd_d(const Problem& p, cudaStream_t s) {
   bp.scale = p.scale;
   bp.causal = p.causal;
   bp.drop = drop_params_of(p);
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, F16, kDrop>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, F16, kDrop, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kBN - 1) / kBN, p.H, p.B);
-  tc_bwd_kernel<D, F16, kDrop><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
+  tc_bwd_kernel<D, F16, kDrop, kDq><<<grid, kThreads, C::kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }
@@ -567,10 +570,23 @@ cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s) {
 
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s) {
   if (p.D == 64) {
-    if (p.dropout) return p.f16 ? launch_bwd_d<64, true, true>(p, s) : launch_bwd_d<64, false, true>(p, s);
-    return p.f16 ? launch_bwd_d<64, true, false>(p, s) : launch_bwd_d<64, false, false>(p, s);
+    if (p.dropout) return p.f16 ? launch_bwd_d<64, true, true, true>(p, s) : launch_bwd_d<64, false, true, true>(p, s);
+    return p.f16 ? launch_bwd_d<64, true, false, true>(p, s) : launch_bwd_d<64, false, false, true>(p, s);
   }
   if (p.D == 128) return launch_tc_bwd128(p, s);
+  return cudaErrorInvalidValue;
+}
+
+// dK and dV without the dQ product (deterministic backward), D = 64 or 128.
+template <int D>
+cudaError_t launch_dkdv_d(const Problem& p, cudaStream_t s) {
+  if (p.dropout) return p.f16 ? launch_bwd_d<D, true, true, false>(p, s) : launch_bwd_d<D, false, true, false>(p, s);
+  return p.f16 ? launch_bwd_d<D, true, false, false>(p, s) : launch_bwd_d<D, false, false, false>(p, s);
+}
+
+cudaError_t launch_tc_bwd_dkdv(const Problem& p, cudaStream_t s) {
+  if (p.D == 64) return launch_dkdv_d<64>(p, s);
+  if (p.D == 128) return launch_dkdv_d<128>(p, s);
   return cudaErrorInvalidValue;
 }
 

@@ -244,6 +244,25 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
                          int causal, const int32_t* cu_seqlens, int total_tokens, fa_dtype dtype, float p_drop,
                          uint64_t seed, uint32_t offset, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Deterministic backward (not on the pages; a variant of the backward's dQ
+ * step): the same gradients as fa_bwd / fa_bwd_dropout, but every sum is taken
+ * in a fixed order, so repeated calls give bit-identical dq, dk, dv.  dK and
+ * dV come from the key-stationary kernel without its dQ product; dQ from a
+ * query-stationary kernel that accumulates each 128-query tile in tensor memory
+ * over the key tiles (recomputing S and dP there) and writes it once, instead
+ * of adding per-key-tile partials into a float32 accumulator.  Costs three more
+ * tile products per (query tile, key tile) pair.
+ * Arguments as fa_bwd_dropout (p_drop = 0: no dropout).  workspace needs only
+ * ceil(rows * 4 / 256) * 256 bytes (rows = B*H*N dense, H*total_tokens packed);
+ * fa_bwd_workspace_size's larger value is accepted too.  float32 inputs run
+ * the float32 path, which is deterministic already (FA_ERR_UNSUPPORTED if
+ * p_drop > 0 there). */
+fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                               float scale, int causal, const int32_t* cu_seqlens, int total_tokens, fa_dtype dtype,
+                               float p_drop, uint64_t seed, uint32_t offset, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
 /* Cached decoding step (tensortonic.com "FlashAttention" section 8: a
  * generation step has a few new queries and a long set of cached keys and
  * values; section 9: the newest query must be aligned with its actual position
