@@ -124,6 +124,7 @@ cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, 
 cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s);
 cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s);  // main kernel only
 cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s);  // main kernel only, D = 128
+cudaError_t launch_tc_bwd128_dkdv(const Problem& p, cudaStream_t s);  // D = 128, dK / dV only
 cudaError_t launch_dq_convert(const Problem& p, cudaStream_t s);  // dQ = bf16(scale * dQ_acc)
 // Deterministic backward: dK / dV (key-stationary, no dQ product) and dQ
 // (query-stationary, accumulated in tensor memory, no atomics).

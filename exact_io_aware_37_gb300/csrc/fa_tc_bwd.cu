@@ -577,7 +577,8 @@ cudaError_t launch_tc_bwd(const Problem& p, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-// dK and dV without the dQ product (deterministic backward), D = 64 or 128.
+// dK and dV without the dQ product (deterministic backward); D = 128 uses the
+// dedicated kernel of fa_tc_bwd128.cu.
 template <int D>
 cudaError_t launch_dkdv_d(const Problem& p, cudaStream_t s) {
   if (p.dropout) return p.f16 ? launch_bwd_d<D, true, true, false>(p, s) : launch_bwd_d<D, false, true, false>(p, s);
@@ -586,7 +587,7 @@ cudaError_t launch_dkdv_d(const Problem& p, cudaStream_t s) {
 
 cudaError_t launch_tc_bwd_dkdv(const Problem& p, cudaStream_t s) {
   if (p.D == 64) return launch_dkdv_d<64>(p, s);
-  if (p.D == 128) return launch_dkdv_d<128>(p, s);
+  if (p.D == 128) return launch_tc_bwd128_dkdv(p, s);
   return cudaErrorInvalidValue;
 }
 

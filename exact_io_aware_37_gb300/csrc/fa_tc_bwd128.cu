@@ -95,7 +95,10 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
 
-template <bool F16, bool kDrop>
+// kDq = false: dK and dV only, for the deterministic backward (whose dQ comes
+// from the query-stationary kernel): no dS^T copy in shared memory, no dQ^T
+// product, read-out or reduction, and dP^T_k waits for nothing but dO_k.
+template <bool F16, bool kDrop, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_constant__ Bwd128Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -266,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
 
-      if (k > 0) drain_dq(k - 1);
+      if constexpr (kDq)
+        if (k > 0) drain_dq(k - 1);
 
       ok = ok && warp_wait(bar_dp, k & 1, w);
       tc_fence_after();
@@ -294,19 +298,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         }
       }
       tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
-      // the dS^T buffer held half 0 of the previous dQ until the copy engine read it
-      if (k > 0) ok = ok && warp_wait(bar_dsfree, (k - 1) & 1, w);
+      if constexpr (kDq) {
+        // the dS^T buffer held half 0 of the previous dQ until the copy engine read it
+        if (k > 0) ok = ok && warp_wait(bar_dsfree, (k - 1) & 1, w);
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)  // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
-        *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) =
-            make_uint4(dsp[4 * c8], dsp[4 * c8 + 1], dsp[4 * c8 + 2], dsp[4 * c8 + 3]);
-      fence_proxy_async_smem();
+        for (int c8 = 0; c8 < 8; ++c8)  // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
+          *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) =
+              make_uint4(dsp[4 * c8], dsp[4 * c8 + 1], dsp[4 * c8 + 2], dsp[4 * c8 + 3]);
+        fence_proxy_async_smem();
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
-    drain_dq(n_steps - 1);
+    if constexpr (kDq) drain_dq(n_steps - 1);
     // epilogue: dV and dK rows of this CTA's keys
     if (ok && warp_wait(bar_done, 0, w)) {
       tc_fence_after();
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         for (int k = max(0, q_issued - 2); k < q_issued; ++k)
           mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
       }
-    } else if (warp == kReduceWarp && lane == 0) {
+    } else if (kDq && warp == kReduceWarp && lane == 0) {
       // ---------------------------------------------------------- dQ reducer
       // Both halves go out back to back; half 0's buffer (the dS^T buffer) is
       // handed back as soon as it has been read, half 1's after that.
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         const bool more = k + 1 < n_steps;
         // dP^T_k over [128,256) once dQ^T_{k-1} has left it (dP^T_0 went out with S^T_0)
         if (k > 0) {
-          if (!mbar_wait(bar_dqfree, (k - 1) & 1, w) || !mbar_wait(bar_of, k & 1, w)) break;
+          if ((kDq && !mbar_wait(bar_dqfree, (k - 1) & 1, w)) || !mbar_wait(bar_of, k & 1, w)) break;
           tc_fence_after();
           issue_dp();
         }
@@ -505,13 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         }
         mma_ts_x8(tmem + 384, at, b, id_acc, acc0);
         mma_commit(bar_qe + st);
+        if constexpr (kDq) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          a[ks] = mK + moff(ks);
-          b[ks] = mDS + moff(ks);
+          for (int ks = 0; ks < 8; ++ks) {
+            a[ks] = mK + moff(ks);
+            b[ks] = mDS + moff(ks);
+          }
+          mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
+          mma_commit(bar_dq);
         }
-        mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
-        mma_commit(bar_dq);
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(bar_done);
@@ -526,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 
 }  // namespace
 
-template <bool F16, bool kDrop>
+template <bool F16, bool kDrop, bool kDq>
 cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   Bwd128Params bp;
   if (!make_map16(&bp.tq, p.q, p, kTile) || !make_map16(&bp.tk, p.k, p, kTile) ||
@@ -548,17 +556,22 @@ cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   bp.scale = p.scale;
   bp.causal = p.causal;
   bp.drop = drop_params_of(p);
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16, kDrop>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16, kDrop, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kTile - 1) / kTile, p.H, p.B);
-  tc_bwd128_kernel<F16, kDrop><<<grid, kThreads, kSmemBytes, s>>>(bp);
+  tc_bwd128_kernel<F16, kDrop, kDq><<<grid, kThreads, kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }
 
 cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
-  if (p.dropout) return p.f16 ? launch_bwd128_t<true, true>(p, s) : launch_bwd128_t<false, true>(p, s);
-  return p.f16 ? launch_bwd128_t<true, false>(p, s) : launch_bwd128_t<false, false>(p, s);
+  if (p.dropout) return p.f16 ? launch_bwd128_t<true, true, true>(p, s) : launch_bwd128_t<false, true, true>(p, s);
+  return p.f16 ? launch_bwd128_t<true, false, true>(p, s) : launch_bwd128_t<false, false, true>(p, s);
+}
+
+cudaError_t launch_tc_bwd128_dkdv(const Problem& p, cudaStream_t s) {
+  if (p.dropout) return p.f16 ? launch_bwd128_t<true, true, false>(p, s) : launch_bwd128_t<false, true, false>(p, s);
+  return p.f16 ? launch_bwd128_t<true, false, false>(p, s) : launch_bwd128_t<false, false, false>(p, s);
 }
 
 }  // namespace fa
