@@ -88,7 +88,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ __align__(8) uint64_t bar_q, bar_done;
-  __shared__ __align__(8) uint64_t bar_k[C::kStages], bar_v[C::kStages], bar_free[C::kStages], bar_step0;
+  // bar_q: both Q tiles and K_0; bar_kv[j % stages]: V_j and K_{j+1} (the two loads one
+  // stage release allows, so the MMA thread waits once per step for its operands)
+  __shared__ __align__(8) uint64_t bar_kv[C::kStages], bar_kfree[C::kStages], bar_vfree[C::kStages];
   __shared__ __align__(8) uint64_t bar_s[2], bar_p[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -127,16 +129,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   nkv[0] = p.causal ? min(qt0 + 1, n_kv) : n_kv;
   nkv[1] = (qt0 + 1 < n_qt) ? (p.causal ? min(qt0 + 2, n_kv) : n_kv) : 0;
   const int nmax = max(nkv[0], nkv[1]);
+  const int t_last = nkv[1] > 0 ? 1 : 0;  // its MMAs are issued last in every step; nkv[t_last] == nmax
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
     mbar_init(&bar_done, 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bar_k[s], 1);
-      mbar_init(&bar_v[s], 1);
-      mbar_init(&bar_free[s], 1);
+      mbar_init(&bar_kv[s], 1);
+      mbar_init(&bar_kfree[s], 1);
+      mbar_init(&bar_vfree[s], 1);
     }
-    mbar_init(&bar_step0, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], 4);  // one arrival per softmax warp
@@ -174,6 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (!warp_wait(&bar_s[t], j & 1, w)) {
           ok = false;
           break;
+        }
+        if (t == t_last && quad == 0 && lane == 0) {
+          // S_t(j) of the last query tile is complete, and with it every MMA issued
+          // before it: S_0(j) (K_j is consumed) and both tiles' P V_{j-1}
+          mbar_arrive(&bar_kfree[j % C::kStages]);
+          if (j > 0) mbar_arrive(&bar_vfree[(j - 1) % C::kStages]);
         }
         tc_fence_after();
         uint32_t sr[4][32];
@@ -287,53 +295,44 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       tma_prefetch_desc(&p.tk);
       tma_prefetch_desc(&p.tv);
       const int nq = nkv[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bar_q, nq * C::kTileBytes);
+      auto load_k = [&](int j, uint64_t* bar) {
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kKOff + (j % C::kStages) * C::kTileBytes + hf * C::kHalfBytes, &p.tk, bar, hf * 64,
+                      row0 + j * kBN, slab);
+      };
+      mbar_arrive_expect_tx(&bar_q, (nq + 1) * C::kTileBytes);
       for (int t = 0; t < nq; ++t)
         for (int hf = 0; hf < C::kHalves; ++hf)
           tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
                       row0 + (qt0 + t) * kBM, slab);
-      // Each mbarrier operation of the MMA thread costs it ~150 clk (and the tensor
-      // pipe the same idle time), so with two stages it commits no per-step
-      // "stage free" barrier: loading
-      // K_j / V_j needs step j - 2 complete, which is completion j - 1 of the S
-      // barrier of the last query tile (completion 0 is the prologue's S_0; its
-      // commit after step i follows every MMA of that step).  A parity wait is
-      // only unambiguous if at least j - 1 and at most j completions can have
-      // happened: at most j holds because completion j needs S(j), i.e. K_j,
-      // which is not loaded yet; at least j - 1 holds from j = 3 on because the
-      // load of j - 1 waited for completion j - 2, and for j = 2 a one-off
-      // barrier committed after step 0 is used instead.
-      const int t_last = nkv[1] > 0 ? 1 : 0;
+      load_k(0, &bar_q);
+      // Stage release: the softmax thread that waits for the last query tile's
+      // S(j) arrives on kfree[j % stages] (K_j consumed: S_0(j) precedes S_1(j))
+      // and on vfree[(j-1) % stages] (both P V_{j-1} precede S_1(j)).  V_j and
+      // K_{j+1} both need the release of softmax step j + 1 - stages, so they
+      // share one barrier, and K runs a step ahead of V without costing the MMA
+      // thread a commit.  Each wait below is unambiguous: the next completion of
+      // the barrier it polls needs a load issued after the wait.
       int issued = 0;
       for (int j = 0; j < nmax; ++j) {
-        const int s = j % C::kStages, round = j / C::kStages;
-        if (round > 0) {
-          bool freed;
-          if (C::kStages != 2)
-            freed = mbar_wait(&bar_free[s], (round - 1) & 1, w);
-          else if (j == 2)
-            freed = mbar_wait(&bar_step0, 0, w);
-          else
-            freed = mbar_wait(&bar_s[t_last], (j - 1) & 1, w);
-          if (!freed) break;
-        }
-        mbar_arrive_expect_tx(&bar_k[s], C::kTileBytes);
+        const int s = j % C::kStages;
+        const bool k_next = j + 1 < nmax;
+        if (j >= C::kStages && !mbar_wait(&bar_vfree[s], (j / C::kStages - 1) & 1, w)) break;
+        if (k_next && j + 1 >= C::kStages &&
+            !mbar_wait(&bar_kfree[(j + 1) % C::kStages], ((j + 1) / C::kStages - 1) & 1, w))
+          break;
+        mbar_arrive_expect_tx(&bar_kv[s], (k_next ? 2 : 1) * C::kTileBytes);
         for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_k[s], hf * 64,
+          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_kv[s], hf * 64,
                       row0 + j * kBN, slab);
-        mbar_arrive_expect_tx(&bar_v[s], C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_v[s], hf * 64,
-                      row0 + j * kBN, slab);
+        if (k_next) load_k(j + 1, &bar_kv[s]);
         issued = j + 1;
       }
       if (abort_flag) {
         // let copies already in flight land before the CTA's memory is released
         mbar_wait_drain(&bar_q, 0, p.limit_ns);
-        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
-          mbar_wait_drain(&bar_k[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
-          mbar_wait_drain(&bar_v[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
-        }
+        for (int j = max(0, issued - C::kStages); j < issued; ++j)
+          mbar_wait_drain(&bar_kv[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -379,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         mma_ts_x8(tmem + 256 + t * 128, a, b, id_o, acc ? 1u : 0u);
       };
-      bool ok = mbar_wait(&bar_q, 0, w) && mbar_wait(&bar_k[0], 0, w);
+      bool ok = mbar_wait(&bar_q, 0, w);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -389,9 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        const int s = j % C::kStages;
-        if (!mbar_wait(&bar_v[s], (j / C::kStages) & 1, w)) break;
-        bool k_next = false;
+        const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
+        // V_j and K_{j+1}
+        if (!mbar_wait(&bar_kv[s], (j / C::kStages) & 1, w)) break;
+        tc_fence_after();
         for (int t = 0; t < 2; ++t) {
           if (j >= nkv[t]) continue;
           if (!mbar_wait(&bar_p[t], j & 1, w)) {
@@ -400,22 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
           tc_fence_after();
           issue_pv(t, s, j > 0);
-          if (j + 1 < nkv[t]) {
-            const int s1 = (j + 1) % C::kStages;
-            if (!k_next) {
-              if (!mbar_wait(&bar_k[s1], ((j + 1) / C::kStages) & 1, w)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_next = true;
-            }
-            issue_s(t, s1);
-          }
+          if (j + 1 < nkv[t]) issue_s(t, s1);
           mma_commit(&bar_s[t]);
         }
-        if (ok && C::kStages != 2) mma_commit(&bar_free[s]);
-        if (ok && C::kStages == 2 && j == 0) mma_commit(&bar_step0);
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(&bar_done);
