@@ -203,7 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       if (lane == 0) mbar_arrive(bar_dqfree);
       // half 1's buffer must have been read by the previous reduction (half 0's
       // buffer is the dS^T buffer, already released before dS^T_kk was written)
-      if (ch == 1 && kk > 0) ok = ok && warp_wait(bar_stfree, (kk - 1) & 1, w);
+      if (ch == 1) {
+        // half 0 goes to the copy engine first and its buffer gates the next dS^T:
+        // let its warps have the shared-memory write bandwidth to themselves
+        ok = ok && warp_wait(bar_staged, kk & 1, w);
+        if (kk > 0) ok = ok && warp_wait(bar_stfree, (kk - 1) & 1, w);
+      }
 #pragma unroll
       for (int e = 0; e < 64; ++e) stage[e * D + j] = __uint_as_float(v[e >> 5][e & 31]);
       fence_proxy_async_smem();
