@@ -20,8 +20,11 @@
 //   The softmax warpgroups raise their register limit to 200 and the third
 //   warpgroup lowers its to 104 (setmaxnreg) so the 128 scores of a row stay
 //   in registers.
-//   warp 8     TMA producer: Q tiles once, then K_j / V_j into a ring of
-//              shared-memory stages (mbarrier full/empty pairs).
+//   warp 8     TMA producer: Q tiles once, then K_j / V_j into rings of
+//              shared-memory stages.  A stage is handed back by the softmax
+//              thread that sees the last query tile's S(j) complete (every
+//              MMA issued before it is then complete too), so K runs a step
+//              ahead of V and the MMA thread commits nothing for it.
 //   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T, then, once the
 //              softmax of tile t has produced P_t, O_t += P_t V_j, then the
 //              next S_t.  The two query tiles alternate so the tensor core
