@@ -59,9 +59,12 @@ struct DqCfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = kTileBytes;
-  static constexpr int kKOff = 2 * kTileBytes;  // + stage * kTileBytes
-  static constexpr int kVOff = 4 * kTileBytes;  // + stage * kTileBytes
-  static constexpr int kSmemBytes = 6 * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kKStages = 3;  // K_j is read until dQ_j, a step after V_j's last reader
+  static constexpr int kVStages = 2;
+  static constexpr int kKOff = 2 * kTileBytes;                  // + stage * kTileBytes
+  static constexpr int kVOff = (2 + kKStages) * kTileBytes;     // + stage * kTileBytes
+  static constexpr int kSmemBytes = (2 + kKStages + kVStages) * kTileBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes + 256 <= 232448, "shared-memory budget");
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -73,7 +76,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_dq_kernel(const __grid_con
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ __align__(8) uint64_t bar_qdo, bar_kv[2], bar_free[2], bar_s, bar_dp, bar_ds, bar_done;
+  __shared__ __align__(8) uint64_t bar_qdo, bar_s, bar_dp, bar_ds, bar_done;
+  __shared__ __align__(8) uint64_t bar_kfull[C::kKStages], bar_kfree[C::kKStages];
+  __shared__ __align__(8) uint64_t bar_vfull[C::kVStages], bar_vfree[C::kVStages];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,9 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_dq_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_qdo, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_kv[s], 1);
-      mbar_init(&bar_free[s], 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&bar_kfull[s], 1);
+      mbar_init(&bar_kfree[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&bar_vfull[s], 1);
+      mbar_init(&bar_vfree[s], 1);
     }
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
@@ -169,6 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_dq_kernel(const __grid_con
         }
       }
       ok = ok && warp_wait(&bar_dp, j & 1, w);
+      if (warp == 0 && lane == 0 && ok) {
+        // dP_j is complete, and with it every MMA issued before it: dQ_{j-1}, the
+        // last reader of K_{j-1}; dP_j itself was V_j's last reader
+        if (j > 0) mbar_arrive(&bar_kfree[(j - 1) % C::kKStages]);
+        mbar_arrive(&bar_vfree[j % C::kVStages]);
+      }
       tc_fence_after();
       tmem_ld32(t_dp, sv[0]);
       tmem_ld32(t_dp + 32, sv[1]);
@@ -232,23 +247,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_dq_kernel(const __grid_con
         tma_load_3d(smem + C::kQOff + hf * C::kHalfBytes, &p.tq, &bar_qdo, hf * 64, row0 + qt * kBM, slab);
         tma_load_3d(smem + C::kDOOff + hf * C::kHalfBytes, &p.tdo, &bar_qdo, hf * 64, row0 + qt * kBM, slab);
       }
-      int issued = 0;
+      // K_j and V_j both become free when a compute thread sees dP_{j+2} or
+      // dP_j complete (K_j's last reader is dQ_j, V_j's is dP_j), i.e. two
+      // steps before the ring needs the stage again.  Each wait polls a
+      // barrier whose next completion needs the load issued after it.
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_steps; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(&bar_free[s], ((j >> 1) - 1) & 1, w)) break;
-        mbar_arrive_expect_tx(&bar_kv[s], 2 * C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_kv[s], hf * 64,
+        const int sk = j % C::kKStages, sv = j % C::kVStages;
+        if (j >= C::kKStages && !mbar_wait(&bar_kfree[sk], (j / C::kKStages - 1) & 1, w)) break;
+        mbar_arrive_expect_tx(&bar_kfull[sk], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kKOff + sk * C::kTileBytes + hf * C::kHalfBytes, &p.tk, &bar_kfull[sk], hf * 64,
                       row0 + j * kBN, slab);
-          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_kv[s], hf * 64,
+        k_issued = j + 1;
+        if (j >= C::kVStages && !mbar_wait(&bar_vfree[sv], (j / C::kVStages - 1) & 1, w)) break;
+        mbar_arrive_expect_tx(&bar_vfull[sv], C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem + C::kVOff + sv * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_vfull[sv], hf * 64,
                       row0 + j * kBN, slab);
-        }
-        issued = j + 1;
+        v_issued = j + 1;
       }
       if (abort_flag) {
         // let copies already in flight land before the CTA's memory is released
         mbar_wait_drain(&bar_qdo, 0, p.limit_ns);
-        for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait_drain(&bar_kv[j & 1], (j >> 1) & 1, p.limit_ns);
+        for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+          mbar_wait_drain(&bar_kfull[j % C::kKStages], (j / C::kKStages) & 1, p.limit_ns);
+        for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+          mbar_wait_drain(&bar_vfull[j % C::kVStages], (j / C::kVStages) & 1, p.limit_ns);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -281,23 +306,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_dq_kernel(const __grid_con
           mma_ss_x4(tmem + d_col, a, bb, id_nn, 0u);
         }
       };
-      bool ok = mbar_wait(&bar_qdo, 0, w) && mbar_wait(&bar_kv[0], 0, w);
+      bool ok = mbar_wait(&bar_qdo, 0, w) && mbar_wait(&bar_kfull[0], 0, w);
       if (ok) {
         tc_fence_after();
         issue_nn(0, kQ, kK);
         mma_commit(&bar_s);
-        issue_nn(256, kDO, kV);
-        mma_commit(&bar_dp);
+        ok = mbar_wait(&bar_vfull[0], 0, w);
+        tc_fence_after();
+        if (ok) {
+          issue_nn(256, kDO, kV);
+          mma_commit(&bar_dp);
+        }
       }
       for (int j = 0; ok && j < n_steps; ++j) {
-        const int s = j & 1, s1 = (j + 1) & 1;
+        const int sk = j % C::kKStages, sk1 = (j + 1) % C::kKStages, sv1 = (j + 1) % C::kVStages;
         const bool more = j + 1 < n_steps;
         // S_{j+1} into the other score region (its previous reader, step j - 1,
         // finished with it before publishing dS_{j-1})
         if (more) {
-          if (!mbar_wait(&bar_kv[s1], ((j + 1) >> 1) & 1, w)) break;
+          if (!mbar_wait(&bar_kfull[sk1], ((j + 1) / C::kKStages) & 1, w)) break;
           tc_fence_after();
-          issue_nn(s1 * 128, kQ, kK + s1 * kStageDesc);
+          issue_nn(((j + 1) & 1) * 128, kQ, kK + sk1 * kStageDesc);
           mma_commit(&bar_s);
         }
         // dQ += dS_j K_j: dS (bf16 pairs) in TMEM columns [256,288) (keys 0-63) and
@@ -310,14 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_dq_kernel(const __grid_con
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             at[ks] = tmem + 256 + (ks >> 2) * 64 + (ks & 3) * 8;
-            bb[ks] = mK + s * kStageDesc + ((ks * 2048) >> 4);
+            bb[ks] = mK + sk * kStageDesc + ((ks * 2048) >> 4);
           }
           mma_ts_x8(tmem + 384, at, bb, id_dq, j > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_free[s]);  // K_j and V_j have no later reader
         // dP_{j+1} over dS_j's columns (dQ_j, issued before, has read them)
         if (more) {
-          issue_nn(256, kDO, kV + s1 * kStageDesc);
+          if (!mbar_wait(&bar_vfull[sv1], ((j + 1) / C::kVStages) & 1, w)) break;
+          tc_fence_after();
+          issue_nn(256, kDO, kV + sv1 * kStageDesc);
           mma_commit(&bar_dp);
         }
       }
