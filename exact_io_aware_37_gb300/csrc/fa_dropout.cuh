@@ -22,20 +22,22 @@ namespace fa {
 struct DropParams {
   uint32_t thr;      // keep iff word >= thr
   float scale;       // 1 / (1 - p)
-  uint32_t seed_lo, seed_hi, offset;
+  uint32_t offset;
+  // The key of round r: (seed mod 2^32, seed / 2^32) advanced r times by the
+  // Weyl increments.  It is the same for every thread, so it is worked out
+  // once on the host and read as a kernel-parameter operand.
+  uint32_t rk0[10], rk1[10];
 };
 
 // Ten rounds; each multiplies words 0 and 2 by the round multipliers into
 // 64-bit products and forms (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
-// lo(M0 c0)); the key advances by the Weyl increments after every round.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// lo(M0 c0)) with the round's key (k0, k1).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const DropParams& d) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
     const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
+    c = make_uint4(hi1 ^ c.y ^ d.rk0[r], lo1, hi0 ^ c.w ^ d.rk1[r], lo0);
   }
   return c;
 }
@@ -43,7 +45,7 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // Keep bits (bit t for key j0 + t) of keys j0 .. j0 + 3 (j0 a multiple of 4)
 // for query row i: one generator call.
 __device__ __forceinline__ uint32_t keep4(const DropParams& d, uint32_t i, uint32_t j0, uint32_t bh) {
-  const uint4 w = philox4x32_10(make_uint4(j0 >> 2, i, bh, d.offset), d.seed_lo, d.seed_hi);
+  const uint4 w = philox4x32_10(make_uint4(j0 >> 2, i, bh, d.offset), d);
   return (w.x >= d.thr ? 1u : 0u) | (w.y >= d.thr ? 2u : 0u) | (w.z >= d.thr ? 4u : 0u) | (w.w >= d.thr ? 8u : 0u);
 }
 
@@ -65,7 +67,7 @@ __device__ __forceinline__ uint64_t keep64_keys_on_lanes(const DropParams& d, ui
   uint64_t bits = 0;
 #pragma unroll 4
   for (int g = 0; g < 16; ++g) {
-    const uint4 w = philox4x32_10(make_uint4(key >> 2, q0 + 4 * g + t, bh, d.offset), d.seed_lo, d.seed_hi);
+    const uint4 w = philox4x32_10(make_uint4(key >> 2, q0 + 4 * g + t, bh, d.offset), d);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const uint32_t send = word_of(w, (t - r) & 3);  // this lane's word for lane (t - r) mod 4
@@ -80,9 +82,12 @@ inline DropParams drop_params_of(const Problem& p) {
   DropParams d;
   d.thr = p.drop_thr;
   d.scale = p.drop_scale;
-  d.seed_lo = (uint32_t)(p.drop_seed & 0xffffffffu);
-  d.seed_hi = (uint32_t)(p.drop_seed >> 32);
   d.offset = p.drop_offset;
+  uint32_t k0 = (uint32_t)(p.drop_seed & 0xffffffffu), k1 = (uint32_t)(p.drop_seed >> 32);
+  for (int r = 0; r < 10; ++r, k0 += 0x9E3779B9u, k1 += 0xBB67AE85u) {
+    d.rk0[r] = k0;
+    d.rk1[r] = k1;
+  }
   return d;
 }
 
