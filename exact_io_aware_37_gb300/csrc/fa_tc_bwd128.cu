@@ -36,6 +36,11 @@
 // warpgroups and 136 for the producer / MMA warpgroup (setmaxnreg).
 #include <math.h>
 
+#include <algorithm>
+#include <mutex>
+#include <queue>
+#include <vector>
+
 #include "fa_dropout.cuh"
 #include "fa_internal.cuh"
 #include "fa_tmap.cuh"
@@ -61,6 +66,22 @@ constexpr int kBwdSupportRegs = 136;
 static_assert(2 * 128 * kBwdComputeRegs + 128 * kBwdSupportRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
 
+// A persistent launch hands each CTA a list of key tiles (b, h, kt) worked
+// out on the host: items in the causal heavy-first order, each given to the
+// CTA with the least work so far (longest processing time first, as the
+// block scheduler would, but without a CTA launch, tensor-memory allocation
+// and pipeline fill per tile: the next tile's loads and first products
+// overlap the previous tile's last reductions and its dK / dV stores).
+constexpr int kMaxSchedCtas = 160;
+constexpr int kMaxSchedItems = 4096;
+
+struct BwdSched {
+  int n_ctas;                         // 0: one key tile per CTA, taken from the grid
+  int n_kt;                           // key tiles per (b, h)
+  uint16_t off[kMaxSchedCtas + 1];    // CTA c works on item[off[c] .. off[c + 1])
+  uint32_t item[kMaxSchedItems];      // (b * H + h) * n_kt + kt
+};
+
 struct Bwd128Params {
   CUtensorMap tq, tk, tv, tdo;
   DropParams drop;  // used by the dropout instantiation only
@@ -76,6 +97,7 @@ struct Bwd128Params {
   float c2;  // scale * log2(e)
   float scale;
   int causal;
+  BwdSched sched;
 };
 
 // Shared memory, dynamic only (1024-byte aligned base, checked).
@@ -90,7 +112,7 @@ constexpr int kStageOff = 6 * kTileBytes;   // dQ staging for queries 64-127: [6
 constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
 constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
 constexpr int kBarOff = kDvOff + 1024;
-constexpr int kNumBars = 18;
+constexpr int kNumBars = 20;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
@@ -122,41 +144,80 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_done = bars + 14;   // every MMA complete
   uint64_t* bar_staged = bars + 15; // [2] dQ half staged in shared memory (4 warps each)
   uint64_t* bar_stfree = bars + 17; // half 1's staging buffer read by the copy engine (reducer)
+  uint64_t* bar_itemdone = bars + 18; // every product of a key tile complete (its dK / dV final, K / V free)
+  uint64_t* bar_accfree = bars + 19;  // dK / dV of a key tile read out of TMEM (8 compute warps)
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
   float* s_l = reinterpret_cast<float*>(smem + kLOff);
   float* s_d = reinterpret_cast<float*>(smem + kDvOff);
 
-  // causal: early key tiles meet the most query tiles and are handed out first
-  const GridItem item = p.causal ? grouped_heavy_first(kBwdHeadGroup) : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
-  const int b = item.b, h = item.h, kt = item.rank;
-  int len, row0, slab;
-  long long out_base;
-  if (p.cu != nullptr) {
-    const int s0 = p.cu[b], s1 = p.cu[b + 1];
-    if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
-      if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
-      return;
-    }
-    len = s1 - s0;
-    row0 = s0;
-    slab = h;
-    out_base = (long long)h * p.T + s0;
-  } else {
-    len = p.N;
-    row0 = 0;
-    slab = b * p.H + h;
-    out_base = (long long)slab * p.N;
+  // ---- the key tiles this CTA works on
+  // Geometry of one key tile: its (b, h) rows and the query tiles that see it.
+  struct Item {
+    int b, h, kt, len, row0, slab, q_first, n_steps;
+    long long out_base;
+  };
+  const bool persistent = p.sched.n_ctas > 0;
+  int n_items = 1, first_item = 0;
+  if (persistent) {
+    first_item = p.sched.off[blockIdx.x];
+    n_items = p.sched.off[blockIdx.x + 1] - first_item;
   }
-  const int n_t = (len + kTile - 1) / kTile;
-  if (kt >= n_t) return;
-  const int q_first = p.causal ? kt : 0;  // earlier query tiles never see these keys
-  const int n_steps = n_t - q_first;
+  auto item_at = [&](int ii) {
+    Item it;
+    if (persistent) {  // dense: every listed tile is in range
+      const uint32_t code = p.sched.item[first_item + ii];
+      const int bh = (int)(code / (uint32_t)p.sched.n_kt);
+      it.kt = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_kt);
+      it.b = bh / p.H;
+      it.h = bh - it.b * p.H;
+      it.len = p.N;
+      it.row0 = 0;
+      it.slab = bh;
+      it.out_base = (long long)bh * p.N;
+    } else {
+      // causal: early key tiles meet the most query tiles and are handed out first
+      const GridItem g = p.causal ? grouped_heavy_first(kBwdHeadGroup)
+                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
+      it.b = g.b;
+      it.h = g.h;
+      it.kt = g.rank;
+      if (p.cu != nullptr) {
+        const int s0 = p.cu[it.b], s1 = p.cu[it.b + 1];
+        it.len = s1 - s0;
+        it.row0 = s0;
+        it.slab = it.h;
+        it.out_base = (long long)it.h * p.T + s0;
+      } else {
+        it.len = p.N;
+        it.row0 = 0;
+        it.slab = it.b * p.H + it.h;
+        it.out_base = (long long)it.slab * p.N;
+      }
+    }
+    const int n_t = (it.len + kTile - 1) / kTile;
+    it.q_first = p.causal ? it.kt : 0;  // earlier query tiles never see these keys
+    it.n_steps = it.kt < n_t ? n_t - it.q_first : 0;
+    return it;
+  };
+  if (!persistent) {
+    if (p.cu != nullptr) {
+      const GridItem g = p.causal ? grouped_heavy_first(kBwdHeadGroup)
+                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
+      const int s0 = p.cu[g.b], s1 = p.cu[g.b + 1];
+      if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
+        if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
+        return;
+      }
+    }
+    if (item_at(0).n_steps <= 0) return;
+  }
+  if (n_items <= 0) return;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint64_t* bar = bars + i;
-      const bool by8 = bar == bar_p || bar == bar_ds || bar == bar_dqfree;
+      const bool by8 = bar == bar_p || bar == bar_ds || bar == bar_dqfree || bar == bar_accfree;
       const bool by4 = bar == bar_staged || bar == bar_staged + 1;
       const bool by2 = bar == bar_qf || bar == bar_qf + 1;  // Q bytes + L / D written
       mbar_init(bar, by8 ? 8 : by4 ? 4 : by2 ? 2 : 1);
@@ -173,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_base_sh;
   const WaitCtx w{abort_flag, p.status, p.limit_ns};
+  // Steps are counted over all of the CTA's key tiles (g = steps of the earlier
+  // tiles + k): every per-step barrier keeps its phase across tiles.
 
   if (warp < 8) {
     // ------------------------------------------------------------ P^T, dS^T, dQ^T read-out, epilogue
@@ -180,7 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     const int ch = warp >> 2;        // query-column half
     const int quad = warp & 3;       // TMEM lanes 32*quad ..
     const int j = quad * 32 + lane;  // key row of S^T / dP^T; head-width column of dQ^T
-    const int key = kt * kTile + j;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + ch * 64;
     const uint32_t t_dp = tmem + lane_off + 128 + ch * 64;  // dP^T, dS^T, then dQ^T of this half
@@ -188,10 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     float* stage = reinterpret_cast<float*>(smem + (ch == 0 ? kDSOff : kStageOff));
     bool ok = true;  // once a wait fails the rest are skipped (the abort flag is set)
 
-    // dQ^T of step kk leaves tensor memory: this warp holds head-width column j
-    // for its half's 64 queries and writes them as rows [64 queries][D] fp32.
-    auto drain_dq = [&](int kk) {
-      ok = ok && warp_wait(bar_dq, kk & 1, w);
+    // dQ^T of global step gg leaves tensor memory: this warp holds head-width
+    // column j for its half's 64 queries and writes them as rows [64 queries][D] fp32.
+    auto drain_dq = [&](int gg) {
+      ok = ok && warp_wait(bar_dq, gg & 1, w);
       tc_fence_after();
       uint32_t v[2][32];
       tmem_ld32(t_dp, v[0]);
@@ -202,12 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
       // half 1's buffer must have been read by the previous reduction (half 0's
-      // buffer is the dS^T buffer, already released before dS^T_kk was written)
+      // buffer is the dS^T buffer, already released before dS^T_gg was written)
       if (ch == 1) {
         // half 0 goes to the copy engine first and its buffer gates the next dS^T:
         // let its warps have the shared-memory write bandwidth to themselves
-        ok = ok && warp_wait(bar_staged, kk & 1, w);
-        if (kk > 0) ok = ok && warp_wait(bar_stfree, (kk - 1) & 1, w);
+        ok = ok && warp_wait(bar_staged, gg & 1, w);
+        if (gg > 0) ok = ok && warp_wait(bar_stfree, (gg - 1) & 1, w);
       }
 #pragma unroll
       for (int e = 0; e < 64; ++e) stage[e * D + j] = __uint_as_float(v[e >> 5][e & 31]);
@@ -216,136 +278,150 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       if (lane == 0) mbar_arrive(bar_staged + ch);
     };
 
-    for (int k = 0; k < n_steps; ++k) {
-      const int qi = q_first + k;
-      const int st = k & 1;
-      const float4* sl4 = reinterpret_cast<const float4*>(s_l + st * 128 + ch * 64);
-      const float4* sd4 = reinterpret_cast<const float4*>(s_d + st * 128 + ch * 64);
-      // dropout decisions of (this half's 64 queries, this key), regenerated
-      uint64_t keepm = ~0ull;
-      if constexpr (kDrop)
-        keepm = keep64_keys_on_lanes(p.drop, (uint32_t)key, (uint32_t)(qi * kTile + ch * 64), (uint32_t)(b * p.H + h),
-                                     lane);
-      ok = ok && warp_wait(bar_qf + st, (k >> 1) & 1, w) && warp_wait(bar_s, k & 1, w);
-      tc_fence_after();
-      uint32_t sv[2][32];
-      tmem_ld32(t_s, sv[0]);
-      tmem_ld32(t_s + 32, sv[1]);
-      tmem_ld_wait(sv[0]);
-      tmem_ld_wait(sv[1]);
-      const int q0 = qi * kTile + ch * 64;  // first query (within the sequence) of this half
-      float pr[64];
+    int G = 0;
+    for (int ii = 0; ok && ii < n_items; ++ii) {
+      const Item it = item_at(ii);
+      const int b = it.b, h = it.h, len = it.len;
+      const int key = it.kt * kTile + j;
+      for (int k = 0; ok && k < it.n_steps; ++k) {
+        const int g = G + k;
+        const int qi = it.q_first + k;
+        const int st = g & 1;
+        const float4* sl4 = reinterpret_cast<const float4*>(s_l + st * 128 + ch * 64);
+        const float4* sd4 = reinterpret_cast<const float4*>(s_d + st * 128 + ch * 64);
+        // dropout decisions of (this half's 64 queries, this key), regenerated
+        uint64_t keepm = ~0ull;
+        if constexpr (kDrop)
+          keepm = keep64_keys_on_lanes(p.drop, (uint32_t)key, (uint32_t)(qi * kTile + ch * 64), (uint32_t)(b * p.H + h),
+                                       lane);
+        ok = ok && warp_wait(bar_qf + st, (g >> 1) & 1, w) && warp_wait(bar_s, g & 1, w);
+        tc_fence_after();
+        uint32_t sv[2][32];
+        tmem_ld32(t_s, sv[0]);
+        tmem_ld32(t_s + 32, sv[1]);
+        tmem_ld_wait(sv[0]);
+        tmem_ld_wait(sv[1]);
+        const int q0 = qi * kTile + ch * 64;  // first query (within the sequence) of this half
+        float pr[64];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = sl4[c4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = sl4[c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int c = 4 * c4 + e;
-          float a0, a1;  // s * scale * log2(e) - L * log2(e), two columns per packed FMA
-          ffma2(a0, a1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]), p.c2,
-                -lv[e], -lv[e + 1]);
-          pr[c] = ex2_approx(a0);
-          pr[c + 1] = ex2_approx(a1);
-        }
-      }
-      if ((p.causal && qi == kt) || (kt * kTile + kTile > len) || (qi * kTile + kTile > len)) {
-        // diagonal or ragged tile: weights of future keys, padding keys and padding queries are zero
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int q = q0 + c;
-          if (q >= len || key >= len || (p.causal && key > q)) pr[c] = 0.f;
-        }
-      }
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if constexpr (kDrop)  // dV takes the dropped weights, scaled by 1 / (1 - p)
-            pk[c] = pack16x2<F16>((keepm >> (2 * c)) & 1 ? pr[2 * c] * p.drop.scale : 0.f,
-                                  (keepm >> (2 * c + 1)) & 1 ? pr[2 * c + 1] * p.drop.scale : 0.f);
-          else
-            pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
-        }
-        tmem_st32(t_s, pk);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
-
-      if constexpr (kDq)
-        if (k > 0) drain_dq(k - 1);
-
-      ok = ok && warp_wait(bar_dp, k & 1, w);
-      tc_fence_after();
-      tmem_ld32(t_dp, sv[0]);
-      tmem_ld32(t_dp + 32, sv[1]);
-      tmem_ld_wait(sv[0]);
-      tmem_ld_wait(sv[1]);
-      uint32_t dsp[32];
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const float4 da = sd4[2 * c8], db = sd4[2 * c8 + 1];
-        const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c8 * 8 + 2 * e;
-          float t0, t1, d0, d1;  // dS = P o (dP - D), two columns per packed op
-          float dp0 = __uint_as_float(sv[c >> 5][c & 31]), dp1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
-          if constexpr (kDrop) {  // dP of the dropped weights: masked and scaled like them
-            dp0 = (keepm >> c) & 1 ? dp0 * p.drop.scale : 0.f;
-            dp1 = (keepm >> (c + 1)) & 1 ? dp1 * p.drop.scale : 0.f;
+          for (int e = 0; e < 4; e += 2) {
+            const int c = 4 * c4 + e;
+            float a0, a1;  // s * scale * log2(e) - L * log2(e), two columns per packed FMA
+            ffma2(a0, a1, __uint_as_float(sv[c >> 5][c & 31]), __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]), p.c2,
+                  -lv[e], -lv[e + 1]);
+            pr[c] = ex2_approx(a0);
+            pr[c + 1] = ex2_approx(a1);
           }
-          fsub2(t0, t1, dp0, dp1, dv[2 * e], dv[2 * e + 1]);
-          fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
-          dsp[4 * c8 + e] = pack16x2<F16>(d0, d1);
         }
-      }
-      tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
-      if constexpr (kDq) {
-        // the dS^T buffer held half 0 of the previous dQ until the copy engine read it
-        if (k > 0) ok = ok && warp_wait(bar_dsfree, (k - 1) & 1, w);
+        if ((p.causal && qi == it.kt) || (it.kt * kTile + kTile > len) || (qi * kTile + kTile > len)) {
+          // diagonal or ragged tile: weights of future keys, padding keys and padding queries are zero
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)  // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
-          *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) =
-              make_uint4(dsp[4 * c8], dsp[4 * c8 + 1], dsp[4 * c8 + 2], dsp[4 * c8 + 3]);
-        fence_proxy_async_smem();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ds);
-    }
-    if constexpr (kDq) drain_dq(n_steps - 1);
-    // epilogue: dV and dK rows of this CTA's keys
-    if (ok && warp_wait(bar_done, 0, w)) {
-      tc_fence_after();
-      const bool row_ok = key < len;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + (out_base + key) * D + ch * 64;
-        const float mul = which == 0 ? 1.f : p.scale;
-        const uint32_t t_acc = tmem + lane_off + (which == 0 ? 256 : 384) + ch * 64;
-#pragma unroll 1
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(t_acc + c, v);
-          tmem_ld_wait(v);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+          for (int c = 0; c < 64; ++c) {
+            const int q = q0 + c;
+            if (q >= len || key >= len || (p.causal && key > q)) pr[c] = 0.f;
+          }
+        }
+        {
+          uint32_t pk[32];
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 u;
-              u.x = pack16x2<F16>(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-              u.y = pack16x2<F16>(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-              u.z = pack16x2<F16>(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-              u.w = pack16x2<F16>(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
-              dst[v4] = u;
+          for (int c = 0; c < 32; ++c) {
+            if constexpr (kDrop)  // dV takes the dropped weights, scaled by 1 / (1 - p)
+              pk[c] = pack16x2<F16>((keepm >> (2 * c)) & 1 ? pr[2 * c] * p.drop.scale : 0.f,
+                                    (keepm >> (2 * c + 1)) & 1 ? pr[2 * c + 1] * p.drop.scale : 0.f);
+            else
+              pk[c] = pack16x2<F16>(pr[2 * c], pr[2 * c + 1]);
+          }
+          tmem_st32(t_s, pk);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p);
+
+        if constexpr (kDq)
+          if (k > 0) drain_dq(g - 1);
+
+        ok = ok && warp_wait(bar_dp, g & 1, w);
+        tc_fence_after();
+        tmem_ld32(t_dp, sv[0]);
+        tmem_ld32(t_dp + 32, sv[1]);
+        tmem_ld_wait(sv[0]);
+        tmem_ld_wait(sv[1]);
+        uint32_t dsp[32];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const float4 da = sd4[2 * c8], db = sd4[2 * c8 + 1];
+          const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c8 * 8 + 2 * e;
+            float t0, t1, d0, d1;  // dS = P o (dP - D), two columns per packed op
+            float dp0 = __uint_as_float(sv[c >> 5][c & 31]), dp1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
+            if constexpr (kDrop) {  // dP of the dropped weights: masked and scaled like them
+              dp0 = (keepm >> c) & 1 ? dp0 * p.drop.scale : 0.f;
+              dp1 = (keepm >> (c + 1)) & 1 ? dp1 * p.drop.scale : 0.f;
+            }
+            fsub2(t0, t1, dp0, dp1, dv[2 * e], dv[2 * e + 1]);
+            fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
+            dsp[4 * c8 + e] = pack16x2<F16>(d0, d1);
+          }
+        }
+        tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
+        if constexpr (kDq) {
+          // the dS^T buffer held half 0 of the previous dQ until the copy engine read it
+          if (g > 0) ok = ok && warp_wait(bar_dsfree, (g - 1) & 1, w);
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)  // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
+            *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) =
+                make_uint4(dsp[4 * c8], dsp[4 * c8 + 1], dsp[4 * c8 + 2], dsp[4 * c8 + 3]);
+          fence_proxy_async_smem();
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ds);
+      }
+      if constexpr (kDq) drain_dq(G + it.n_steps - 1);
+      // epilogue: dV and dK rows of this tile's keys, once its last products are complete
+      if (ok && warp_wait(bar_itemdone, ii & 1, w)) {
+        tc_fence_after();
+        const bool row_ok = key < len;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + (it.out_base + key) * D + ch * 64;
+          const float mul = which == 0 ? 1.f : p.scale;
+          const uint32_t t_acc = tmem + lane_off + (which == 0 ? 256 : 384) + ch * 64;
+#pragma unroll 1
+          for (int c = 0; c < 64; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(t_acc + c, v);
+            tmem_ld_wait(v);
+            if (which == 1 && c == 32) {
+              // the accumulators are read: the next tile's dV / dK may start over them
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_accfree);
+            }
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 u;
+                u.x = pack16x2<F16>(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
+                u.y = pack16x2<F16>(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
+                u.z = pack16x2<F16>(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
+                u.w = pack16x2<F16>(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
+                dst[v4] = u;
+              }
             }
           }
         }
       }
+      G += it.n_steps;
     }
   } else {
     setmaxnreg_dec<kBwdSupportRegs>();
@@ -356,79 +432,133 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         tma_prefetch_desc(&p.tk);
         tma_prefetch_desc(&p.tv);
         tma_prefetch_desc(&p.tdo);
-        mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_load_3d(smem + kKOff + hf * kHalfBytes, &p.tk, bar_kv, hf * 64, row0 + kt * kTile, slab);
-          tma_load_3d(smem + kVOff + hf * kHalfBytes, &p.tv, bar_kv, hf * 64, row0 + kt * kTile, slab);
-        }
       }
-      int q_issued = 0, o_issued = 0;
-      for (int k = 0; k < n_steps; ++k) {
-        const int qi = q_first + k;
-        const int st = k & 1;
-        // Q / L / D stage st was last used by step k - 2 (free once its dK has
-        // completed); the single dO buffer by step k - 1 (free once its dV has).
-        // Lane 0 waits and the answer is broadcast, so the warp never splits.
-        // L and D of the tile are fetched before the wait, so the Q copy goes out
-        // as soon as its stage is free; the stage's barrier takes a second
-        // arrival once they are in shared memory.
-        float lv[4], dv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int qrow = qi * kTile + lane * 4 + e;
-          const bool in = qrow < len;
-          lv[e] = in ? p.lse[out_base + qrow] * kLog2e : 0.f;
-          dv[e] = in ? p.dvec[out_base + qrow] : 0.f;
-        }
+      int q_issued = 0, o_issued = 0, kv_issued = 0, G = 0;
+      bool good_all = true;
+      // K, V of a tile, once every product of the previous tile (their last
+      // readers) is complete; lane 0 waits, the answer is broadcast
+      auto load_kv = [&](const Item& it, int ii) {
         int good = 1;
-        if (lane == 0 && k >= 2) good = mbar_wait(bar_qe + st, ((k >> 1) - 1) & 1, w);
-        if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar_qf + st, kTileBytes);
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
-                        row0 + qi * kTile, slab);
+          if (ii > 0) good = mbar_wait(bar_itemdone, (ii - 1) & 1, w);
+          if (good) {
+            mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
+            for (int hf = 0; hf < 2; ++hf) {
+              tma_load_3d(smem + kKOff + hf * kHalfBytes, &p.tk, bar_kv, hf * 64, it.row0 + it.kt * kTile, it.slab);
+              tma_load_3d(smem + kVOff + hf * kHalfBytes, &p.tv, bar_kv, hf * 64, it.row0 + it.kt * kTile, it.slab);
+            }
+          }
         }
-        q_issued = k + 1;
-        *reinterpret_cast<float4*>(s_l + st * 128 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
-        *reinterpret_cast<float4*>(s_d + st * 128 + lane * 4) = make_float4(dv[0], dv[1], dv[2], dv[3]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_qf + st);
-        if (lane == 0 && k >= 1) good = mbar_wait(bar_oe, (k - 1) & 1, w);
-        if (!__shfl_sync(0xffffffffu, good, 0)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar_of, kTileBytes);
-          for (int hf = 0; hf < 2; ++hf)
-            tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, row0 + qi * kTile, slab);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (good) kv_issued = ii + 1;
+        return good != 0;
+      };
+      for (int ii = 0; good_all && ii < n_items; ++ii) {
+        const Item it = item_at(ii);
+        // The first tile's K and V go first; a later tile's wait until its first
+        // Q, L / D and dO are on their way, which need no more than their buffers.
+        if (ii == 0 && !load_kv(it, ii)) break;
+        int good = 1;
+        for (int k = 0; k < it.n_steps; ++k) {
+          const int g = G + k;
+          const int qi = it.q_first + k;
+          const int st = g & 1;
+          // Q / L / D stage st was last used by step g - 2 (free once its dK has
+          // completed); the single dO buffer by step g - 1 (free once its dV has).
+          // Lane 0 waits and the answer is broadcast, so the warp never splits.
+          // L and D of the tile are fetched before the wait, so the Q copy goes out
+          // as soon as its stage is free; the stage's barrier takes a second
+          // arrival once they are in shared memory.
+          float lv[4], dv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int qrow = qi * kTile + lane * 4 + e;
+            const bool in = qrow < it.len;
+            lv[e] = in ? p.lse[it.out_base + qrow] * kLog2e : 0.f;
+            dv[e] = in ? p.dvec[it.out_base + qrow] : 0.f;
+          }
+          if (lane == 0 && g >= 2) good = mbar_wait(bar_qe + st, ((g >> 1) - 1) & 1, w);
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            good_all = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar_qf + st, kTileBytes);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
+                          it.row0 + qi * kTile, it.slab);
+          }
+          q_issued = g + 1;
+          *reinterpret_cast<float4*>(s_l + st * 128 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
+          *reinterpret_cast<float4*>(s_d + st * 128 + lane * 4) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_qf + st);
+          if (lane == 0 && g >= 1) good = mbar_wait(bar_oe, (g - 1) & 1, w);
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            good_all = false;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar_of, kTileBytes);
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, it.row0 + qi * kTile, it.slab);
+          }
+          o_issued = g + 1;
+          if (k == 0 && ii > 0 && !load_kv(it, ii)) {
+            good_all = false;
+            break;
+          }
         }
-        o_issued = k + 1;
+        // the next tile's K and V wait for this tile's last products; have them
+        // in L2 by then
+        if (lane == 0 && ii + 1 < n_items) {
+          const Item nx = item_at(ii + 1);
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_prefetch_l2_3d(&p.tk, hf * 64, nx.row0 + nx.kt * kTile, nx.slab);
+            tma_prefetch_l2_3d(&p.tv, hf * 64, nx.row0 + nx.kt * kTile, nx.slab);
+          }
+        }
+        G += it.n_steps;
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
-        mbar_wait_drain(bar_kv, 0, p.limit_ns);
+        if (kv_issued > 0) mbar_wait_drain(bar_kv, (kv_issued - 1) & 1, p.limit_ns);
         if (o_issued > 0) mbar_wait_drain(bar_of, (o_issued - 1) & 1, p.limit_ns);
-        for (int k = max(0, q_issued - 2); k < q_issued; ++k)
-          mbar_wait_drain(bar_qf + (k & 1), (k >> 1) & 1, p.limit_ns);
+        for (int g = max(0, q_issued - 2); g < q_issued; ++g)
+          mbar_wait_drain(bar_qf + (g & 1), (g >> 1) & 1, p.limit_ns);
       }
     } else if (kDq && warp == kReduceWarp && lane == 0) {
       // ---------------------------------------------------------- dQ reducer
       // Both halves go out back to back; half 0's buffer (the dS^T buffer) is
       // handed back as soon as it has been read, half 1's after that.
-      for (int kk = 0; kk < n_steps; ++kk) {
-        const int q0 = (q_first + kk) * kTile;
-        for (int hf = 0; hf < 2; ++hf) {
-          if (!mbar_wait(bar_staged + hf, kk & 1, w)) break;
-          const int nq = min(64, len - (q0 + hf * 64));
-          if (nq > 0)
-            bulk_reduce_add_f32(p.dq_acc + (out_base + q0 + hf * 64) * D, smem + (hf == 0 ? kDSOff : kStageOff),
-                                (uint32_t)nq * D * 4);
-          bulk_commit();
+      int G = 0;
+      bool good = true;
+      for (int ii = 0; good && ii < n_items; ++ii) {
+        const Item it = item_at(ii);
+        for (int kk = 0; good && kk < it.n_steps; ++kk) {
+          const int gg = G + kk;
+          const int q0 = (it.q_first + kk) * kTile;
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(bar_staged + hf, gg & 1, w)) {
+              good = false;
+              break;
+            }
+            const int nq = min(64, it.len - (q0 + hf * 64));
+            if (nq > 0)
+              bulk_reduce_add_f32(p.dq_acc + (it.out_base + q0 + hf * 64) * D, smem + (hf == 0 ? kDSOff : kStageOff),
+                                  (uint32_t)nq * D * 4);
+            bulk_commit();
+          }
+          if (!good || *abort_flag) {
+            good = false;
+            break;
+          }
+          bulk_wait_read<1>();  // half 0 read
+          mbar_arrive(bar_dsfree);
+          bulk_wait_read<0>();  // half 1 read
+          mbar_arrive(bar_stfree);
         }
-        if (*abort_flag) break;
-        bulk_wait_read<1>();  // half 0 read
-        mbar_arrive(bar_dsfree);
-        bulk_wait_read<0>();  // half 1 read
-        mbar_arrive(bar_stfree);
+        G += it.n_steps;
       }
       bulk_wait_all();
     } else if (warp == kMmaWarp && lane == 0) {
@@ -452,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       // Each group of 8 MMAs is issued back to back from one asm block.
       uint64_t a[8], b[8];
       uint32_t at[8];
-      auto issue_s = [&](int k) {  // S^T_k = K Q_k^T -> [0,128)
-        const int st = k & 1;
+      auto issue_s = [&](int g) {  // S^T of global step g = K Q_g^T -> [0,128)
+        const int st = g & 1;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           a[ks] = kK + koff(ks);
@@ -462,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         mma_ss_x8(tmem + 0, a, b, id_nn, 0u);
         mma_commit(bar_s);
       };
-      auto issue_dp = [&]() {  // dP^T_k = V dO_k^T -> [128,256)
+      auto issue_dp = [&]() {  // dP^T = V dO^T -> [128,256)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           a[ks] = kV + koff(ks);
@@ -471,60 +601,95 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         mma_ss_x8(tmem + 128, a, b, id_nn, 0u);
         mma_commit(bar_dp);
       };
-      bool ok = mbar_wait(bar_kv, 0, w) && mbar_wait(bar_qf, 0, w);
-      if (ok) {
+      bool ok = true;
+      int G = 0;
+      // the step count of each tile, worked out without the rest of its geometry
+      // (this thread has few registers to spare)
+      const int n_steps0 = item_at(0).n_steps;
+      for (int ii = 0; ok && ii < n_items; ++ii) {
+        int n_steps = n_steps0;
+        if (persistent) {
+          const uint32_t code = p.sched.item[first_item + ii];
+          const int kt = (int)(code % (uint32_t)p.sched.n_kt);
+          n_steps = p.causal ? p.sched.n_kt - kt : p.sched.n_kt;
+        }
+        // K, V of this tile; S^T and dP^T of its first step.  dP^T goes over the
+        // previous tile's last dQ^T, so it waits until that has been read out.
+        ok = mbar_wait(bar_kv, ii & 1, w) && mbar_wait(bar_qf + (G & 1), (G >> 1) & 1, w);
+        if (!ok) break;
         tc_fence_after();
-        issue_s(0);
-        ok = mbar_wait(bar_of, 0, w);
+        issue_s(G);
+        ok = (!kDq || G == 0 || mbar_wait(bar_dqfree, (G - 1) & 1, w)) && mbar_wait(bar_of, G & 1, w);
+        if (!ok) break;
         tc_fence_after();
-        if (ok) issue_dp();
-      }
-      for (int k = 0; ok && k < n_steps; ++k) {
-        const int st = k & 1;
-        const uint32_t acc0 = k > 0 ? 1u : 0u;
-        const bool more = k + 1 < n_steps;
-        // dP^T_k over [128,256) once dQ^T_{k-1} has left it (dP^T_0 went out with S^T_0)
-        if (k > 0) {
-          if ((kDq && !mbar_wait(bar_dqfree, (k - 1) & 1, w)) || !mbar_wait(bar_of, k & 1, w)) break;
+        issue_dp();
+        for (int k = 0; ok && k < n_steps; ++k) {
+          const int g = G + k;
+          const int st = g & 1;
+          const uint32_t acc0 = k > 0 ? 1u : 0u;
+          const bool more = k + 1 < n_steps;
+          // dP^T over [128,256) once the previous dQ^T has left it
+          if (k > 0) {
+            if ((kDq && !mbar_wait(bar_dqfree, (g - 1) & 1, w)) || !mbar_wait(bar_of, g & 1, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_dp();
+          }
+          // dV += P^T dO: P^T (bf16) in TMEM columns [0,32) (queries 0-63) and [64,96);
+          // the tile's first dV / dK start over accumulators the previous tile's
+          // epilogue must have read
+          if (!mbar_wait(bar_p, g & 1, w) || (k == 0 && ii > 0 && !mbar_wait(bar_accfree, (ii - 1) & 1, w))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_dp();
-        }
-        // dV += P^T dO: P^T (bf16) in TMEM columns [0,32) (queries 0-63) and [64,96)
-        if (!mbar_wait(bar_p, k & 1, w)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          at[ks] = tmem + (ks >> 2) * 64 + (ks & 3) * 8;
-          b[ks] = mDO + moff(ks);
-        }
-        mma_ts_x8(tmem + 256, at, b, id_acc, acc0);
-        mma_commit(bar_oe);  // dP^T_k and dV_k were the dO tile's last readers
-        // S^T of the next step over the score columns (P^T is consumed in order by dV)
-        if (more) {
-          if (!mbar_wait(bar_qf + (st ^ 1), ((k + 1) >> 1) & 1, w)) break;
-          tc_fence_after();
-          issue_s(k + 1);
-        }
-        // dK += dS^T Q (dS^T bf16 in TMEM columns [128,160) and [192,224)), then
-        // dQ^T = K^T dS^T over [128,256) (dS^T MN-major from shared memory)
-        if (!mbar_wait(bar_ds, k & 1, w)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          at[ks] = tmem + 128 + (ks >> 2) * 64 + (ks & 3) * 8;
-          b[ks] = mQ + st * kStageDesc + moff(ks);
-        }
-        mma_ts_x8(tmem + 384, at, b, id_acc, acc0);
-        mma_commit(bar_qe + st);
-        if constexpr (kDq) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            a[ks] = mK + moff(ks);
-            b[ks] = mDS + moff(ks);
+            at[ks] = tmem + (ks >> 2) * 64 + (ks & 3) * 8;
+            b[ks] = mDO + moff(ks);
           }
-          mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
-          mma_commit(bar_dq);
+          mma_ts_x8(tmem + 256, at, b, id_acc, acc0);
+          mma_commit(bar_oe);  // dP^T and dV were the dO tile's last readers
+          // S^T of the next step over the score columns (P^T is consumed in order by dV)
+          if (more) {
+            if (!mbar_wait(bar_qf + (st ^ 1), ((g + 1) >> 1) & 1, w)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(g + 1);
+          }
+          // dK += dS^T Q (dS^T bf16 in TMEM columns [128,160) and [192,224)), then
+          // dQ^T = K^T dS^T over [128,256) (dS^T MN-major from shared memory)
+          if (!mbar_wait(bar_ds, g & 1, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            at[ks] = tmem + 128 + (ks >> 2) * 64 + (ks & 3) * 8;
+            b[ks] = mQ + st * kStageDesc + moff(ks);
+          }
+          mma_ts_x8(tmem + 384, at, b, id_acc, acc0);
+          mma_commit(bar_qe + st);
+          if constexpr (kDq) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              a[ks] = mK + moff(ks);
+              b[ks] = mDS + moff(ks);
+            }
+            mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
+            mma_commit(bar_dq);
+          }
         }
+        if (!ok) break;
+        // the tile's dK / dV are final, and K / V have no later reader, once
+        // every product issued so far is complete
+        mma_commit(bar_itemdone);
+        G += n_steps;
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(bar_done);
@@ -539,9 +704,94 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 
 }  // namespace
 
+// Multiprocessor count of the current device.
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Per-tile cost, in steps, of what a persistent CTA does for a key tile besides
+// its steps (the K / V load it waits for, the epilogue); it only steers the
+// balance of the schedule.
+constexpr int kItemOverheadSteps = 2;
+
+// Schedule of a persistent launch for dense inputs: false (no schedule, one
+// CTA per key tile) for packed inputs, whose tile sizes live on the device, or
+// when the tiles do not fit the parameter block.
+bool build_sched(const Problem& p, BwdSched& sc) {
+  sc.n_ctas = 0;
+  const int n_kt = (p.N + kTile - 1) / kTile;
+  const long long n_bh = (long long)p.B * p.H;
+  const long long n = n_bh * n_kt;
+  const int sms = sm_count();
+  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || sms <= 0) return false;
+  const int ctas = (int)std::min<long long>(n, std::min(sms, kMaxSchedCtas));
+  static std::mutex mu;
+  static long long key[5] = {-1, -1, -1, -1, -1};
+  static BwdSched cached;
+  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  std::lock_guard<std::mutex> lock(mu);
+  if (std::equal(want, want + 5, key)) {
+    sc = cached;
+    return true;
+  }
+  // Items in the order the grid used: with the mask, heavy-first inside
+  // balanced groups of kBwdHeadGroup heads (the order of grouped_heavy_first).
+  std::vector<uint32_t> order((size_t)n);
+  std::vector<int> weight((size_t)n);
+  const long long n_groups = (n_bh + kBwdHeadGroup - 1) / kBwdHeadGroup;
+  const long long per = (n_bh + n_groups - 1) / n_groups;
+  for (long long f = 0; f < n; ++f) {
+    long long bh, kt;
+    if (p.causal) {
+      const long long group = f / (per * n_kt), r = f - group * per * n_kt;
+      const long long heads = std::min(per, n_bh - group * per);
+      bh = group * per + r % heads;
+      kt = r / heads;
+    } else {
+      bh = f / n_kt;
+      kt = f % n_kt;
+    }
+    order[(size_t)f] = (uint32_t)(bh * n_kt + kt);
+    weight[(size_t)f] = (p.causal ? (int)(n_kt - kt) : n_kt) + kItemOverheadSteps;
+  }
+  // Each item to the CTA with the least work so far (lowest index on ties).
+  using Slot = std::pair<long long, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  std::vector<std::vector<uint32_t>> lists((size_t)ctas);
+  for (long long f = 0; f < n; ++f) {
+    Slot t = heap.top();
+    heap.pop();
+    lists[(size_t)t.second].push_back(order[(size_t)f]);
+    t.first += weight[(size_t)f];
+    heap.push(t);
+  }
+  int at = 0;
+  for (int c = 0; c < ctas; ++c) {
+    sc.off[c] = (uint16_t)at;
+    for (uint32_t code : lists[(size_t)c]) sc.item[at++] = code;
+  }
+  sc.off[ctas] = (uint16_t)at;
+  sc.n_ctas = ctas;
+  sc.n_kt = n_kt;
+  cached = sc;
+  std::copy(want, want + 5, key);
+  return true;
+}
+
 template <bool F16, bool kDrop, bool kDq>
 cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
-  Bwd128Params bp;
+  static Bwd128Params bp;  // large (the schedule); filled in full below on every call
+  static std::mutex launch_mu;
+  std::lock_guard<std::mutex> launch_lock(launch_mu);
   if (!make_map16(&bp.tq, p.q, p, kTile) || !make_map16(&bp.tk, p.k, p, kTile) ||
       !make_map16(&bp.tv, p.v, p, kTile) || !make_map16(&bp.tdo, p.dout, p, kTile))
     return note_error("backward tensor map encode", cudaErrorInvalidValue);
@@ -564,6 +814,7 @@ cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16, kDrop, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
   dim3 grid((p.N + kTile - 1) / kTile, p.H, p.B);
+  if (build_sched(p, bp.sched)) grid = dim3(bp.sched.n_ctas, 1, 1);
   tc_bwd128_kernel<F16, kDrop, kDq><<<grid, kThreads, kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
