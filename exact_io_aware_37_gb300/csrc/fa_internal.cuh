@@ -105,6 +105,9 @@ __device__ __forceinline__ void st_elem(float* p, long long i, float x) { p[i] =
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, long long i, float x) { p[i] = __float2bfloat16_rn(x); }
 __device__ __forceinline__ void st_elem(__half* p, long long i, float x) { p[i] = __float2half_rn(x); }
 
+// Multiprocessor count of the current device (0 if it cannot be read); cached.
+int sm_count();
+
 // Counts kernel launches (read by fa_launch_count); every launcher bumps it.
 void note_launches(unsigned n);
 

@@ -38,6 +38,11 @@
 // O_1 [384,384+D); P_t (bf16 pairs) overwrites S_t columns [0,64).
 #include <math.h>
 
+#include <algorithm>
+#include <mutex>
+#include <queue>
+#include <vector>
+
 #include "fa_dropout.cuh"
 #include "fa_internal.cuh"
 #include "fa_tmap.cuh"
@@ -56,6 +61,20 @@ constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kFwdHeadGroup = 16;  // heads per group of the causal block order (measured best of 8..64)
 
+// A persistent launch hands each CTA a list of query-tile pairs worked out on
+// the host (the causal heavy-first order, each pair to the CTA with the least
+// work so far), so the CTA launch, tensor-memory allocation and first loads
+// are paid once per CTA and a pair's epilogue overlaps the next pair's loads.
+constexpr int kMaxSchedCtas = 160;
+constexpr int kMaxSchedItems = 4096;
+
+struct FwdSched {
+  int n_ctas;                       // 0: one pair per CTA, taken from the grid
+  int n_pairs;                      // pairs per (b, h)
+  uint16_t off[kMaxSchedCtas + 1];  // CTA c works on item[off[c] .. off[c + 1])
+  uint32_t item[kMaxSchedItems];    // (b * H + h) * n_pairs + pair
+};
+
 struct FwdParams {
   CUtensorMap tq, tk, tv;
   DropParams drop;  // used by the dropout instantiation only
@@ -67,6 +86,7 @@ struct FwdParams {
   int B, H, N, T;
   float c2;  // scale * log2(e)
   int causal;
+  FwdSched sched;
 };
 
 template <int D>
@@ -90,52 +110,90 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ __align__(8) uint64_t bar_q, bar_done;
-  // bar_q: both Q tiles and K_0; bar_kv[j % stages]: V_j and K_{j+1} (the two loads one
-  // stage release allows, so the MMA thread waits once per step for its operands)
+  // bar_q: a pair's Q tiles (the first pair's also K_0); bar_kv[g % stages]: V_g and
+  // K_{g+1} (the two loads one stage release allows, so the MMA thread waits once
+  // per step for its operands; K_{g+1} may be the next pair's K_0).  Steps g are
+  // counted over all of the CTA's pairs, so every ring and per-step barrier keeps
+  // its phase from one pair to the next.
+  __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_done;
   __shared__ __align__(8) uint64_t bar_kv[C::kStages], bar_kfree[C::kStages], bar_vfree[C::kStages];
-  __shared__ __align__(8) uint64_t bar_s[2], bar_p[2];
+  __shared__ __align__(8) uint64_t bar_s[2], bar_p[2], bar_epi[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // causal: pairs of late query tiles see the most keys and are handed out first
-  const GridItem item = p.causal ? grouped_heavy_first(kFwdHeadGroup) : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
-  const int b = item.b, h = item.h;
 
-  // ---- the (sequence, head) this CTA works on
-  int len, row0, slab;
-  long long out_base;
-  if (p.cu != nullptr) {
-    const int s0 = p.cu[b], s1 = p.cu[b + 1];
-    if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
-      if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
-      return;
-    }
-    len = s1 - s0;
-    row0 = s0;
-    slab = h;
-    out_base = (long long)h * p.T + s0;
-  } else {
-    len = p.N;
-    row0 = 0;
-    slab = b * p.H + h;
-    out_base = (long long)slab * p.N;
+  // ---- the query-tile pairs this CTA works on
+  struct Pair {
+    int b, h, len, row0, slab, qt0, nkv0, nkv1, nmax, t_last;
+    long long out_base;
+  };
+  const bool persistent = p.sched.n_ctas > 0;
+  int n_items = 1, first_item = 0;
+  if (persistent) {
+    first_item = p.sched.off[blockIdx.x];
+    n_items = p.sched.off[blockIdx.x + 1] - first_item;
   }
-  const int n_qt = (len + kBM - 1) / kBM;
-  const int n_pairs = (n_qt + 1) / 2;
-  const int pair = p.causal ? (int)gridDim.x - 1 - item.rank : item.rank;
-  if (pair >= n_pairs) return;
-  const int qt0 = 2 * pair;
-  const int n_kv = (len + kBN - 1) / kBN;
-  int nkv[2];
-  nkv[0] = p.causal ? min(qt0 + 1, n_kv) : n_kv;
-  nkv[1] = (qt0 + 1 < n_qt) ? (p.causal ? min(qt0 + 2, n_kv) : n_kv) : 0;
-  const int nmax = max(nkv[0], nkv[1]);
-  const int t_last = nkv[1] > 0 ? 1 : 0;  // its MMAs are issued last in every step; nkv[t_last] == nmax
+  auto pair_at = [&](int ii) {
+    Pair q;
+    int pair;
+    if (persistent) {  // dense: every listed pair is in range
+      const uint32_t code = p.sched.item[first_item + ii];
+      const int bh = (int)(code / (uint32_t)p.sched.n_pairs);
+      pair = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_pairs);
+      q.b = bh / p.H;
+      q.h = bh - q.b * p.H;
+      q.len = p.N;
+      q.row0 = 0;
+      q.slab = bh;
+      q.out_base = (long long)bh * p.N;
+    } else {
+      // causal: pairs of late query tiles see the most keys and are handed out first
+      const GridItem g = p.causal ? grouped_heavy_first(kFwdHeadGroup)
+                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
+      q.b = g.b;
+      q.h = g.h;
+      pair = p.causal ? (int)gridDim.x - 1 - g.rank : g.rank;
+      if (p.cu != nullptr) {
+        const int s0 = p.cu[q.b], s1 = p.cu[q.b + 1];
+        q.len = s1 - s0;
+        q.row0 = s0;
+        q.slab = q.h;
+        q.out_base = (long long)q.h * p.T + s0;
+      } else {
+        q.len = p.N;
+        q.row0 = 0;
+        q.slab = q.b * p.H + q.h;
+        q.out_base = (long long)q.slab * p.N;
+      }
+    }
+    const int n_qt = (q.len + kBM - 1) / kBM;
+    const int n_kv = (q.len + kBN - 1) / kBN;
+    q.qt0 = 2 * pair;
+    const bool in = pair < (n_qt + 1) / 2;
+    q.nkv0 = !in ? 0 : p.causal ? min(q.qt0 + 1, n_kv) : n_kv;
+    q.nkv1 = (in && q.qt0 + 1 < n_qt) ? (p.causal ? min(q.qt0 + 2, n_kv) : n_kv) : 0;
+    q.nmax = max(q.nkv0, q.nkv1);
+    q.t_last = q.nkv1 > 0 ? 1 : 0;  // its MMAs are issued last in every step; its count is nmax
+    return q;
+  };
+  if (!persistent) {
+    if (p.cu != nullptr) {
+      const GridItem g = p.causal ? grouped_heavy_first(kFwdHeadGroup)
+                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
+      const int s0 = p.cu[g.b], s1 = p.cu[g.b + 1];
+      if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
+        if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
+        return;
+      }
+    }
+    if (pair_at(0).nmax <= 0) return;
+  }
+  if (n_items <= 0) return;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_qfree, 1);
     mbar_init(&bar_done, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bar_kv[s], 1);
@@ -144,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s[t], 1);
-      mbar_init(&bar_p[t], 4);  // one arrival per softmax warp
+      mbar_init(&bar_p[t], 4);    // one arrival per softmax warp
+      mbar_init(&bar_epi[t], 4);  // the tile's softmax warps have seen its last P V complete
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -165,129 +224,149 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const int t = warp >> 2;
     const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
     const int r = quad * 32 + lane;     // row within the query tile
-    const int qt = qt0 + t;
-    const int n = nkv[t];
-    if (n > 0) {
-      const int i = qt * kBM + r;       // row within the sequence
-      const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-      const uint32_t t_s = tmem + lane_off + t * 128;
-      const uint32_t t_o = tmem + lane_off + 256 + t * 128;
-      float m_ref = -INFINITY;          // reference maximum of the exponentials (log2 units)
-      float l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        if (!warp_wait(&bar_s[t], j & 1, w)) {
-          ok = false;
-          break;
-        }
-        if (t == t_last && quad == 0 && lane == 0) {
-          // S_t(j) of the last query tile is complete, and with it every MMA issued
-          // before it: S_0(j) (K_j is consumed) and both tiles' P V_{j-1}
-          mbar_arrive(&bar_kfree[j % C::kStages]);
-          if (j > 0) mbar_arrive(&bar_vfree[(j - 1) % C::kStages]);
-        }
-        tc_fence_after();
-        uint32_t sr[4][32];
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + t * 128;
+    const uint32_t t_o = tmem + lane_off + 256 + t * 128;
+    bool ok = true;
+    int G = 0;   // steps of the earlier pairs
+    int cs = 0;  // completions of bar_s[t] seen so far
+    for (int ii = 0; ok && ii < n_items; ++ii) {
+      const Pair q = pair_at(ii);
+      const int n = t == 0 ? q.nkv0 : q.nkv1;
+      const int len = q.len;
+      if (n > 0) {
+        const int qt = q.qt0 + t;
+        const int i = qt * kBM + r;       // row within the sequence
+        float m_ref = -INFINITY;          // reference maximum of the exponentials (log2 units)
+        float l = 0.f;
+        for (int j = 0; j < n; ++j) {
+          const int g = G + j;
+          if (!warp_wait(&bar_s[t], cs & 1, w)) {
+            ok = false;
+            break;
+          }
+          ++cs;
+          if (t == q.t_last && quad == 0 && lane == 0) {
+            // S_t(j) of the last query tile is complete, and with it every MMA issued
+            // before it: S_0(j) (K_g is consumed), both tiles' P V of the step before
+            // (V_{g-1}, possibly the previous pair's last V) and, at the pair's last
+            // step, every S of the pair (its Q tiles are free)
+            mbar_arrive(&bar_kfree[g % C::kStages]);
+            if (g > 0) mbar_arrive(&bar_vfree[(g - 1) % C::kStages]);
+            if (j == n - 1) mbar_arrive(&bar_qfree);
+          }
+          tc_fence_after();
+          uint32_t sr[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
+          for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
-        const int k0 = j * kBN;
-        if ((p.causal && j == qt) || (k0 + kBN > len)) {
-          // diagonal or ragged tile: keys [k0, k0 + kmax) are allowed, the rest get -inf
-          const int kmax = min(len, p.causal ? i + 1 : len) - k0;
+          for (int c = 0; c < 4; ++c) tmem_ld_wait(sr[c]);
+          const int k0 = j * kBN;
+          if ((p.causal && j == qt) || (k0 + kBN > len)) {
+            // diagonal or ragged tile: keys [k0, k0 + kmax) are allowed, the rest get -inf
+            const int kmax = min(len, p.causal ? i + 1 : len) - k0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (c * 32 + e >= kmax) sr[c][e] = __float_as_uint(-INFINITY);
+          }
+          // row maximum of the raw scores (scale > 0 preserves the order)
+          float mt = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e >= kmax) sr[c][e] = __float_as_uint(-INFINITY);
-        }
-        // row maximum of the raw scores (scale > 0 preserves the order)
-        float mt = -INFINITY;
+            for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          const float m_new = fmaxf(m_ref, mt * p.c2);
+          float alpha = 1.f;
+          const bool grow = m_new > m_ref + kRescaleThreshold;
+          if (grow) {
+            alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+            l *= alpha;
+          }
+          const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
+          // p = 2^(s * scale * log2(e) - m_ref), two columns per packed FMA
+          float rs0 = 0.f, rs1 = 0.f;
+          uint32_t kbits = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
-        const float m_new = fmaxf(m_ref, mt * p.c2);
-        float alpha = 1.f;
-        const bool grow = m_new > m_ref + kRescaleThreshold;
-        if (grow) {
-          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
-          m_ref = m_new;
-          l *= alpha;
-        }
-        const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
-        // p = 2^(s * scale * log2(e) - m_ref), two columns per packed FMA
-        float rs0 = 0.f, rs1 = 0.f;
-        uint32_t kbits = 0;
+            for (int c = 0; c < 32; ++c) {
+              const int e0 = 64 * hf + 2 * c;
+              float a0, a1;
+              ffma2(a0, a1, __uint_as_float(sr[e0 >> 5][e0 & 31]), __uint_as_float(sr[(e0 + 1) >> 5][(e0 + 1) & 31]),
+                    p.c2, nmu, nmu);
+              const float p0 = ex2_approx(a0);
+              const float p1 = ex2_approx(a1);
+              fadd2(rs0, rs1, p0, p1);  // the normaliser is that of the undropped weights
+              if constexpr (kDrop) {
+                // dropped weights enter PV scaled by 1 / (1 - p); one generator call per 4 keys
+                if ((c & 1) == 0)
+                  kbits = keep4(p.drop, (uint32_t)i, (uint32_t)(k0 + e0), (uint32_t)(q.b * p.H + q.h));
+                const uint32_t sh = (c & 1) * 2;
+                pk[c] = pack16x2<F16>((kbits >> sh) & 1u ? p0 * p.drop.scale : 0.f,
+                                      (kbits >> (sh + 1)) & 1u ? p1 * p.drop.scale : 0.f);
+              } else {
+                pk[c] = pack16x2<F16>(p0, p1);
+              }
+            }
+            tmem_st32(t_s + 32 * hf, pk);
+          }
+          l += rs0 + rs1;
+          if (j > 0 && __any_sync(0xffffffffu, grow)) {
+            // accumulator rows rescaled in place: the previous PV is complete (the
+            // wait on bar_s covers it) and this tile's PV waits for bar_p below
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(t_o + c, o);
+              tmem_ld_wait(o);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int e0 = 64 * hf + 2 * c;
-            float a0, a1;
-            ffma2(a0, a1, __uint_as_float(sr[e0 >> 5][e0 & 31]), __uint_as_float(sr[(e0 + 1) >> 5][(e0 + 1) & 31]),
-                  p.c2, nmu, nmu);
-            const float p0 = ex2_approx(a0);
-            const float p1 = ex2_approx(a1);
-            fadd2(rs0, rs1, p0, p1);  // the normaliser is that of the undropped weights
-            if constexpr (kDrop) {
-              // dropped weights enter PV scaled by 1 / (1 - p); one generator call per 4 keys
-              if ((c & 1) == 0) kbits = keep4(p.drop, (uint32_t)i, (uint32_t)(k0 + e0), (uint32_t)(b * p.H + h));
-              const uint32_t sh = (c & 1) * 2;
-              pk[c] = pack16x2<F16>((kbits >> sh) & 1u ? p0 * p.drop.scale : 0.f,
-                                    (kbits >> (sh + 1)) & 1u ? p1 * p.drop.scale : 0.f);
-            } else {
-              pk[c] = pack16x2<F16>(p0, p1);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(t_o + c, o);
             }
           }
-          tmem_st32(t_s + 32 * hf, pk);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_p[t]);
         }
-        l += rs0 + rs1;
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // accumulator rows rescaled in place: the previous PV is complete (the
-          // wait on bar_s covers it) and this tile's PV waits for bar_p below
+        if (ok && warp_wait(&bar_s[t], cs & 1, w)) {
+          ++cs;
+          // the tile's last P V is complete: the MMA thread may start the next
+          // pair's S over this tile's score columns
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_epi[t]);
+          tc_fence_after();
+          const bool row_ok = i < len;
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          __nv_bfloat16* orow = p.o + (q.out_base + i) * D;
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
             tmem_ld32(t_o + c, o);
             tmem_ld_wait(o);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_o + c, o);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p[t]);
-      }
-      if (ok && warp_wait(&bar_s[t], n & 1, w)) {
-        tc_fence_after();
-        const bool row_ok = i < len;
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + (out_base + i) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(t_o + c, o);
-          tmem_ld_wait(o);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 u;
-              u.x = pack16x2<F16>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-              u.y = pack16x2<F16>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-              u.z = pack16x2<F16>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-              u.w = pack16x2<F16>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-              dst[v4] = u;
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint4 u;
+                u.x = pack16x2<F16>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                u.y = pack16x2<F16>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                u.z = pack16x2<F16>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                u.w = pack16x2<F16>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                dst[v4] = u;
+              }
             }
           }
+          if (row_ok) p.lse[q.out_base + i] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+        } else {
+          ok = false;
         }
-        if (row_ok) p.lse[out_base + i] = l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       }
+      G += q.nmax;
     }
   } else {
     // warps 8-11: producer, MMA issuer and two idle warps completing the warpgroup
@@ -297,45 +376,77 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       tma_prefetch_desc(&p.tq);
       tma_prefetch_desc(&p.tk);
       tma_prefetch_desc(&p.tv);
-      const int nq = nkv[1] > 0 ? 2 : 1;
-      auto load_k = [&](int j, uint64_t* bar) {
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kKOff + (j % C::kStages) * C::kTileBytes + hf * C::kHalfBytes, &p.tk, bar, hf * 64,
-                      row0 + j * kBN, slab);
+      auto load_q = [&](const Pair& q, int extra) {
+        const int nq = q.nkv1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(&bar_q, (nq + extra) * C::kTileBytes);
+        for (int t = 0; t < nq; ++t)
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
+                        q.row0 + (q.qt0 + t) * kBM, q.slab);
       };
-      mbar_arrive_expect_tx(&bar_q, (nq + 1) * C::kTileBytes);
-      for (int t = 0; t < nq; ++t)
+      auto load_k = [&](const Pair& q, int j, int g, uint64_t* bar) {
         for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &p.tq, &bar_q, hf * 64,
-                      row0 + (qt0 + t) * kBM, slab);
-      load_k(0, &bar_q);
+          tma_load_3d(smem + C::kKOff + (g % C::kStages) * C::kTileBytes + hf * C::kHalfBytes, &p.tk, bar, hf * 64,
+                      q.row0 + j * kBN, q.slab);
+      };
       // Stage release: the softmax thread that waits for the last query tile's
-      // S(j) arrives on kfree[j % stages] (K_j consumed: S_0(j) precedes S_1(j))
-      // and on vfree[(j-1) % stages] (both P V_{j-1} precede S_1(j)).  V_j and
-      // K_{j+1} both need the release of softmax step j + 1 - stages, so they
-      // share one barrier, and K runs a step ahead of V without costing the MMA
-      // thread a commit.  Each wait below is unambiguous: the next completion of
+      // S(g) arrives on kfree[g % stages] (K_g consumed: S_0 precedes S_1) and on
+      // vfree[(g-1) % stages] (both P V of step g - 1 precede S_1(g)).  V_g and
+      // K_{g+1} both need the release of step g + 1 - stages, so they share one
+      // barrier, and K runs a step ahead of V without costing the MMA thread a
+      // commit.  A pair's Q tiles go out once the previous pair's every S is
+      // complete (qfree).  Each wait below is unambiguous: the next completion of
       // the barrier it polls needs a load issued after the wait.
-      int issued = 0;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % C::kStages;
-        const bool k_next = j + 1 < nmax;
-        if (j >= C::kStages && !mbar_wait(&bar_vfree[s], (j / C::kStages - 1) & 1, w)) break;
-        if (k_next && j + 1 >= C::kStages &&
-            !mbar_wait(&bar_kfree[(j + 1) % C::kStages], ((j + 1) / C::kStages - 1) & 1, w))
-          break;
-        mbar_arrive_expect_tx(&bar_kv[s], (k_next ? 2 : 1) * C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_kv[s], hf * 64,
-                      row0 + j * kBN, slab);
-        if (k_next) load_k(j + 1, &bar_kv[s]);
-        issued = j + 1;
+      int issued = 0, q_issued = 0, G = 0;
+      bool good = true;
+      Pair q = pair_at(0);
+      load_q(q, 1);
+      load_k(q, 0, 0, &bar_q);
+      q_issued = 1;
+      for (int ii = 0; good && ii < n_items; ++ii) {
+        const bool has_next = ii + 1 < n_items;
+        const Pair nx = has_next ? pair_at(ii + 1) : q;
+        for (int j = 0; j < q.nmax; ++j) {
+          const int g = G + j;
+          const int s = g % C::kStages;
+          // K_{g+1}: this pair's next K, or the next pair's K_0
+          const bool k_next = j + 1 < q.nmax || has_next;
+          if (g >= C::kStages && !mbar_wait(&bar_vfree[s], (g / C::kStages - 1) & 1, w)) {
+            good = false;
+            break;
+          }
+          if (k_next && g + 1 >= C::kStages &&
+              !mbar_wait(&bar_kfree[(g + 1) % C::kStages], ((g + 1) / C::kStages - 1) & 1, w)) {
+            good = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bar_kv[s], (k_next ? 2 : 1) * C::kTileBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(smem + C::kVOff + s * C::kTileBytes + hf * C::kHalfBytes, &p.tv, &bar_kv[s], hf * 64,
+                        q.row0 + j * kBN, q.slab);
+          if (k_next) {
+            if (j + 1 < q.nmax)
+              load_k(q, j + 1, g + 1, &bar_kv[s]);
+            else
+              load_k(nx, 0, g + 1, &bar_kv[s]);
+          }
+          issued = g + 1;
+        }
+        if (!good) break;
+        G += q.nmax;
+        if (has_next) {
+          // the next pair's Q tiles over this pair's, once every S of this pair is complete
+          if (!mbar_wait(&bar_qfree, ii & 1, w)) break;
+          load_q(nx, 0);
+          q_issued = ii + 2;
+        }
+        q = nx;
       }
       if (abort_flag) {
         // let copies already in flight land before the CTA's memory is released
-        mbar_wait_drain(&bar_q, 0, p.limit_ns);
-        for (int j = max(0, issued - C::kStages); j < issued; ++j)
-          mbar_wait_drain(&bar_kv[j % C::kStages], (j / C::kStages) & 1, p.limit_ns);
+        if (q_issued > 0) mbar_wait_drain(&bar_q, (q_issued - 1) & 1, p.limit_ns);
+        for (int g = max(0, issued - C::kStages); g < issued; ++g)
+          mbar_wait_drain(&bar_kv[g % C::kStages], (g / C::kStages) & 1, p.limit_ns);
       }
     } else if (warp == kMmaWarp && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -381,31 +492,60 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         mma_ts_x8(tmem + 256 + t * 128, a, b, id_o, acc ? 1u : 0u);
       };
-      bool ok = mbar_wait(&bar_q, 0, w);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0) {
-            issue_s(t, 0);
-            mma_commit(&bar_s[t]);
-          }
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
-        // V_j and K_{j+1}
-        if (!mbar_wait(&bar_kv[s], (j / C::kStages) & 1, w)) break;
+      bool ok = true;
+      int G = 0;
+      int cp[2] = {0, 0};    // completions of bar_p[t] waited for
+      int used[2] = {0, 0};  // pairs that used query tile t so far
+      for (int ii = 0; ok && ii < n_items; ++ii) {
+        // the pair's step counts, without the rest of its geometry (this thread
+        // has few registers to spare)
+        int nk[2];
+        {
+          const Pair q = pair_at(ii);
+          nk[0] = q.nkv0;
+          nk[1] = q.nkv1;
+        }
+        const int nmax = max(nk[0], nk[1]);
+        // Q tiles (and, for the first pair, K_0; later pairs' K_0 came with the
+        // previous pair's last V, whose barrier was waited for); each tile's S goes
+        // over score columns its softmax warps must have finished with
+        ok = mbar_wait(&bar_q, ii & 1, w);
+        if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t) {
-          if (j >= nkv[t]) continue;
-          if (!mbar_wait(&bar_p[t], j & 1, w)) {
+          if (nk[t] == 0) continue;
+          if (used[t] > 0 && !mbar_wait(&bar_epi[t], (used[t] - 1) & 1, w)) {
+            ok = false;
+            break;
+          }
+          ++used[t];
+          tc_fence_after();
+          issue_s(t, G % C::kStages);
+          mma_commit(&bar_s[t]);
+        }
+        for (int j = 0; ok && j < nmax; ++j) {
+          const int g = G + j;
+          const int s = g % C::kStages, s1 = (g + 1) % C::kStages;
+          // V_g and K_{g+1}
+          if (!mbar_wait(&bar_kv[s], (g / C::kStages) & 1, w)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(t, s, j > 0);
-          if (j + 1 < nkv[t]) issue_s(t, s1);
-          mma_commit(&bar_s[t]);
+          for (int t = 0; t < 2; ++t) {
+            if (j >= nk[t]) continue;
+            if (!mbar_wait(&bar_p[t], cp[t] & 1, w)) {
+              ok = false;
+              break;
+            }
+            ++cp[t];
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            if (j + 1 < nk[t]) issue_s(t, s1);
+            mma_commit(&bar_s[t]);
+          }
         }
+        G += nmax;
       }
       // every MMA issued must be complete before tensor memory is released
       mma_commit(&bar_done);
@@ -418,10 +558,83 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
+// Per-pair cost, in steps, of what a persistent CTA does besides the pair's
+// steps (waiting for its Q tiles, the epilogue); it only steers the balance.
+constexpr int kPairOverheadSteps = 1;
+
+// Schedule of a persistent launch for dense inputs: false (one CTA per pair)
+// for packed inputs, whose sequence lengths live on the device, or when the
+// pairs do not fit the parameter block.
+bool build_fwd_sched(const Problem& p, FwdSched& sc) {
+  sc.n_ctas = 0;
+  const int n_qt = (p.N + kBM - 1) / kBM, n_kv = (p.N + kBN - 1) / kBN;
+  const int n_pairs = (n_qt + 1) / 2;
+  const long long n_bh = (long long)p.B * p.H;
+  const long long n = n_bh * n_pairs;
+  const int sms = sm_count();
+  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || sms <= 0) return false;
+  const int ctas = (int)std::min<long long>(n, std::min(sms, kMaxSchedCtas));
+  static std::mutex mu;
+  static long long key[5] = {-1, -1, -1, -1, -1};
+  static FwdSched cached;
+  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  std::lock_guard<std::mutex> lock(mu);
+  if (std::equal(want, want + 5, key)) {
+    sc = cached;
+    return true;
+  }
+  // Pairs in the order the grid used: with the mask, heaviest first inside
+  // balanced groups of kFwdHeadGroup heads (the order of grouped_heavy_first).
+  std::vector<uint32_t> order((size_t)n);
+  std::vector<int> weight((size_t)n);
+  const long long n_groups = (n_bh + kFwdHeadGroup - 1) / kFwdHeadGroup;
+  const long long per = (n_bh + n_groups - 1) / n_groups;
+  for (long long f = 0; f < n; ++f) {
+    long long bh, pair;
+    if (p.causal) {
+      const long long group = f / (per * n_pairs), r = f - group * per * n_pairs;
+      const long long heads = std::min(per, n_bh - group * per);
+      bh = group * per + r % heads;
+      pair = n_pairs - 1 - r / heads;
+    } else {
+      bh = f / n_pairs;
+      pair = f % n_pairs;
+    }
+    order[(size_t)f] = (uint32_t)(bh * n_pairs + pair);
+    const int steps = p.causal ? std::min((int)(2 * pair + 2), n_kv) : n_kv;
+    weight[(size_t)f] = steps + kPairOverheadSteps;
+  }
+  // Each pair to the CTA with the least work so far (lowest index on ties).
+  using Slot = std::pair<long long, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < ctas; ++c) heap.push({0, c});
+  std::vector<std::vector<uint32_t>> lists((size_t)ctas);
+  for (long long f = 0; f < n; ++f) {
+    Slot t = heap.top();
+    heap.pop();
+    lists[(size_t)t.second].push_back(order[(size_t)f]);
+    t.first += weight[(size_t)f];
+    heap.push(t);
+  }
+  int at = 0;
+  for (int c = 0; c < ctas; ++c) {
+    sc.off[c] = (uint16_t)at;
+    for (uint32_t code : lists[(size_t)c]) sc.item[at++] = code;
+  }
+  sc.off[ctas] = (uint16_t)at;
+  sc.n_ctas = ctas;
+  sc.n_pairs = n_pairs;
+  cached = sc;
+  std::copy(want, want + 5, key);
+  return true;
+}
+
 template <int D, bool F16, bool kDrop>
 cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   using C = FwdCfg<D>;
-  FwdParams fp;
+  static FwdParams fp;  // large (the schedule); filled in full below on every call
+  static std::mutex launch_mu;
+  std::lock_guard<std::mutex> launch_lock(launch_mu);
   if (!make_map16(&fp.tq, p.q, p, kBM) || !make_map16(&fp.tk, p.k, p, kBN) ||
       !make_map16(&fp.tv, p.v, p, kBN))
     return note_error("forward tensor map encode", cudaErrorInvalidValue);
@@ -441,6 +654,7 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   if (e != cudaSuccess) return note_error("forward smem attribute", e);
   const int n_qt = (p.N + kBM - 1) / kBM;
   dim3 grid((n_qt + 1) / 2, p.H, p.B);
+  if (build_fwd_sched(p, fp.sched)) grid = dim3(fp.sched.n_ctas, 1, 1);
   tc_fwd_kernel<D, F16, kDrop><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
   note_launches(1);
   return note_error("forward launch", cudaGetLastError());
