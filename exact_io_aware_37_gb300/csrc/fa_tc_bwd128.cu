@@ -4,8 +4,10 @@
 // Same method as the D = 64 kernel (tensortonic.com "FlashAttention",
 // section 7: every weight is rebuilt as P_ij = exp(s_ij - L_i) from the
 // saved log-sum-exp; dV = P^T dO, dS = P o (dO V^T - D), dK = scale dS^T Q,
-// dQ = scale dS K): a CTA owns one 128-key tile of K and V in shared memory
-// and visits the 128-query tiles that can see it.  All five products are
+// dQ = scale dS K): a CTA holds one 128-key tile of K and V in shared memory
+// at a time and visits the 128-query tiles that can see it; for dense inputs
+// it is persistent and works through a host-built list of key tiles (see
+// BwdSched).  All five products are
 // tcgen05 MMAs with M = N = 128, placed in tensor memory as
 //     [0,128)   S^T = K Q^T, then P^T (bf16) over its columns [0,32) and [64,96)
 //     [128,256) dP^T = V dO^T, then dS^T (bf16) over [128,160) and [192,224),

@@ -2,8 +2,10 @@
 //
 // The method is the query-first tiled schedule of tensortonic.com
 // "FlashAttention" section 6 with the running softmax of section 5: a CTA
-// owns two 128-row query tiles of one (sequence, head), loads them once, and
-// visits the allowed 128-key K/V tiles in turn.  The score tile and the
+// works on two 128-row query tiles of one (sequence, head) at a time (a
+// pair), loads them once, and visits the allowed 128-key K/V tiles in turn;
+// for dense inputs it is persistent and works through a host-built list of
+// pairs (see FwdSched).  The score tile and the
 // output accumulator never leave the SM: S = Q K^T and u += P V are tcgen05
 // MMAs whose accumulators live in tensor memory (TMEM), and only O = u / l and
 // L = m + log(l) are written to device memory (section 7).
