@@ -161,6 +161,21 @@ const char* fa_path_name(fa_dtype dt, int D) {
 
 unsigned long long fa_launch_count(void) { return g_launches.load(); }
 
+int fa_schedule_preview(int kernel, int B, int H, int N, int causal, int n_ctas, unsigned short* off,
+                        unsigned int* items, int cap) {
+  if ((kernel != 0 && kernel != 1) || B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1) || n_ctas <= 0 ||
+      off == nullptr || cap < 0 || (items == nullptr && cap > 0))
+    return -1;
+  fa::Problem p{};
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal;
+  p.cu = nullptr;
+  return kernel == 0 ? fa::preview_fwd_schedule(p, n_ctas, off, items, cap)
+                     : fa::preview_bwd_schedule(p, n_ctas, off, items, cap);
+}
+
 const char* fa_last_error_detail(void) { return g_detail; }
 
 void fa_bwd_time_main_kernel(void* start_event, void* stop_event) {

@@ -108,6 +108,11 @@ __device__ __forceinline__ void st_elem(__half* p, long long i, float x) { p[i] 
 // Multiprocessor count of the current device (0 if it cannot be read); cached.
 int sm_count();
 
+// Work lists of the persistent forward / backward launches for `ctas` CTAs
+// (host only; see fa_schedule_preview).
+int preview_fwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap);
+int preview_bwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap);
+
 // Counts kernel launches (read by fa_launch_count); every launcher bumps it.
 void note_launches(unsigned n);
 

@@ -724,26 +724,16 @@ int sm_count() {
 // balance of the schedule.
 constexpr int kItemOverheadSteps = 2;
 
-// Schedule of a persistent launch for dense inputs: false (no schedule, one
-// CTA per key tile) for packed inputs, whose tile sizes live on the device, or
-// when the tiles do not fit the parameter block.
-bool build_sched(const Problem& p, BwdSched& sc) {
+// The work list for at most `ctas_max` CTAs: false (no schedule, one CTA per
+// key tile) for packed inputs, whose tile sizes live on the device, or when
+// the tiles do not fit the parameter block.
+bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
   sc.n_ctas = 0;
   const int n_kt = (p.N + kTile - 1) / kTile;
   const long long n_bh = (long long)p.B * p.H;
   const long long n = n_bh * n_kt;
-  const int sms = sm_count();
-  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || sms <= 0) return false;
-  const int ctas = (int)std::min<long long>(n, std::min(sms, kMaxSchedCtas));
-  static std::mutex mu;
-  static long long key[5] = {-1, -1, -1, -1, -1};
-  static BwdSched cached;
-  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
-  std::lock_guard<std::mutex> lock(mu);
-  if (std::equal(want, want + 5, key)) {
-    sc = cached;
-    return true;
-  }
+  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || ctas_max <= 0) return false;
+  const int ctas = (int)std::min<long long>(n, std::min(ctas_max, kMaxSchedCtas));
   // Items in the order the grid used: with the mask, heavy-first inside
   // balanced groups of kBwdHeadGroup heads (the order of grouped_heavy_first).
   std::vector<uint32_t> order((size_t)n);
@@ -784,9 +774,38 @@ bool build_sched(const Problem& p, BwdSched& sc) {
   sc.off[ctas] = (uint16_t)at;
   sc.n_ctas = ctas;
   sc.n_kt = n_kt;
+  return true;
+}
+
+// The schedule of a launch on the current device (one CTA per SM), cached for
+// the last problem shape.
+bool build_sched(const Problem& p, BwdSched& sc) {
+  const int ctas = sm_count();
+  static std::mutex mu;
+  static long long key[5] = {-1, -1, -1, -1, -1};
+  static BwdSched cached;
+  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  std::lock_guard<std::mutex> lock(mu);
+  if (p.cu == nullptr && std::equal(want, want + 5, key)) {
+    sc = cached;
+    return true;
+  }
+  if (!fill_bwd_sched(p, ctas, sc)) return false;
   cached = sc;
   std::copy(want, want + 5, key);
   return true;
+}
+
+int preview_bwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap) {
+  static BwdSched sc;  // large; previews are a host-side test aid
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fill_bwd_sched(p, ctas, sc)) return -1;
+  const int n = sc.off[sc.n_ctas];
+  if (n > cap) return -2;
+  std::copy(sc.off, sc.off + sc.n_ctas + 1, off);
+  std::copy(sc.item, sc.item + n, items);
+  return n;
 }
 
 template <bool F16, bool kDrop, bool kDq>

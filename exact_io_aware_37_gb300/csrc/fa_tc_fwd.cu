@@ -564,27 +564,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 // steps (waiting for its Q tiles, the epilogue); it only steers the balance.
 constexpr int kPairOverheadSteps = 1;
 
-// Schedule of a persistent launch for dense inputs: false (one CTA per pair)
-// for packed inputs, whose sequence lengths live on the device, or when the
-// pairs do not fit the parameter block.
-bool build_fwd_sched(const Problem& p, FwdSched& sc) {
+// The work list for at most `ctas_max` CTAs: false (one CTA per pair) for
+// packed inputs, whose sequence lengths live on the device, or when the pairs
+// do not fit the parameter block.
+bool fill_fwd_sched(const Problem& p, int ctas_max, FwdSched& sc) {
   sc.n_ctas = 0;
   const int n_qt = (p.N + kBM - 1) / kBM, n_kv = (p.N + kBN - 1) / kBN;
   const int n_pairs = (n_qt + 1) / 2;
   const long long n_bh = (long long)p.B * p.H;
   const long long n = n_bh * n_pairs;
-  const int sms = sm_count();
-  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || sms <= 0) return false;
-  const int ctas = (int)std::min<long long>(n, std::min(sms, kMaxSchedCtas));
-  static std::mutex mu;
-  static long long key[5] = {-1, -1, -1, -1, -1};
-  static FwdSched cached;
-  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
-  std::lock_guard<std::mutex> lock(mu);
-  if (std::equal(want, want + 5, key)) {
-    sc = cached;
-    return true;
-  }
+  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || ctas_max <= 0) return false;
+  const int ctas = (int)std::min<long long>(n, std::min(ctas_max, kMaxSchedCtas));
   // Pairs in the order the grid used: with the mask, heaviest first inside
   // balanced groups of kFwdHeadGroup heads (the order of grouped_heavy_first).
   std::vector<uint32_t> order((size_t)n);
@@ -626,6 +616,23 @@ bool build_fwd_sched(const Problem& p, FwdSched& sc) {
   sc.off[ctas] = (uint16_t)at;
   sc.n_ctas = ctas;
   sc.n_pairs = n_pairs;
+  return true;
+}
+
+// The schedule of a launch on the current device (one CTA per SM), cached for
+// the last problem shape.
+bool build_fwd_sched(const Problem& p, FwdSched& sc) {
+  const int ctas = sm_count();
+  static std::mutex mu;
+  static long long key[5] = {-1, -1, -1, -1, -1};
+  static FwdSched cached;
+  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  std::lock_guard<std::mutex> lock(mu);
+  if (p.cu == nullptr && std::equal(want, want + 5, key)) {
+    sc = cached;
+    return true;
+  }
+  if (!fill_fwd_sched(p, ctas, sc)) return false;
   cached = sc;
   std::copy(want, want + 5, key);
   return true;
@@ -663,6 +670,18 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+int preview_fwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap) {
+  static FwdSched sc;  // large; previews are a host-side test aid
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fill_fwd_sched(p, ctas, sc)) return -1;
+  const int n = sc.off[sc.n_ctas];
+  if (n > cap) return -2;
+  std::copy(sc.off, sc.off + sc.n_ctas + 1, off);
+  std::copy(sc.item, sc.item + n, items);
+  return n;
+}
 
 cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s) {
   if (p.dropout) {

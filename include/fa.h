@@ -220,6 +220,23 @@ void fa_bwd_time_main_kernel(void* start_event, void* stop_event);
  */
 unsigned long long fa_launch_count(void);
 
+/*
+ * Host-only view of the work list a persistent launch uses for dense inputs
+ * of B x H x N (instrumentation and tests; no GPU needed).  kernel 0 = the
+ * tensor-core forward, whose items are pairs of 128-row query tiles,
+ * code = (b * H + h) * n_pairs + pair; kernel 1 = the D = 128 backward,
+ * whose items are 128-key tiles, code = (b * H + h) * n_kt + kt.  The items
+ * are taken in the order the one-CTA-per-item grid would hand them out and
+ * each goes to the CTA with the least work so far; at most min(n_ctas, 160)
+ * CTAs get work.  Writes off[0 .. c] (off must hold n_ctas + 1 entries;
+ * CTA i works on items[off[i] .. off[i + 1]), in that order) and returns the
+ * number of items; -1 for arguments out of range or problems too large for a
+ * persistent launch (more than 4096 items), -2 if `cap` is below the item
+ * count.
+ */
+int fa_schedule_preview(int kernel, int B, int H, int N, int causal, int n_ctas, unsigned short* off,
+                        unsigned int* items, int cap);
+
 /* Attention dropout (tensortonic.com "FlashAttention" section 7: the backward
  * must reproduce the forward's dropout decisions from saved generator state).
  * Same arguments as fa_fwd / fa_bwd plus:

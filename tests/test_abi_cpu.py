@@ -176,3 +176,53 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.lib()
+
+
+# Work lists of the persistent launches (host logic, no GPU).  Weights are the
+# per-item step counts plus the per-item overheads the schedulers charge:
+# 1 step for a forward query-tile pair, 2 for a backward key tile.
+def _preview(lib, kernel, B, H, N, causal, ctas):
+    off = (ctypes.c_ushort * (ctas + 1))()
+    cap = 4096
+    items = (ctypes.c_uint * cap)()
+    n = lib.fa_schedule_preview(kernel, B, H, N, causal, ctas, off, items, cap)
+    return n, list(off), list(items[:max(n, 0)])
+
+
+def _weights(kernel, H, B, N, causal):
+    n_t = (N + 127) // 128
+    if kernel == 0:
+        n_pairs = (n_t + 1) // 2
+        per = [(min(2 * pr + 2, n_t) if causal else n_t) + 1 for pr in range(n_pairs)]
+    else:
+        per = [(n_t - kt if causal else n_t) + 2 for kt in range(n_t)]
+    return {bh * len(per) + u: w for bh in range(B * H) for u, w in enumerate(per)}
+
+
+@pytest.mark.parametrize("kernel,B,H,N,causal,ctas", [
+    (0, 2, 32, 4096, 1, 152), (0, 2, 32, 4096, 0, 152), (1, 2, 32, 4096, 1, 152), (1, 2, 32, 4096, 0, 152),
+    (0, 4, 16, 1024, 1, 152), (1, 4, 16, 1024, 1, 152), (0, 1, 3, 300, 1, 152), (1, 1, 3, 300, 0, 7),
+    (0, 1, 32, 32768, 1, 152), (1, 2, 5, 2000, 1, 64)])
+def test_persistent_schedule_covers_and_balances(lib, kernel, B, H, N, causal, ctas):
+    n, off, items = _preview(lib, kernel, B, H, N, causal, ctas)
+    weight = _weights(kernel, H, B, N, causal)
+    assert n == len(weight)
+    # every item exactly once
+    assert sorted(items) == sorted(weight)
+    used = min(ctas, 160, n)
+    assert off[0] == 0 and off[used] == n
+    assert all(off[c] <= off[c + 1] for c in range(used))
+    loads = [sum(weight[code] for code in items[off[c]:off[c + 1]]) for c in range(used)]
+    # greedy assignment to the least-loaded CTA: no CTA ends more than one item heavier than another
+    assert max(loads) - min(loads) <= max(weight.values())
+    # and no CTA gets more than one item above the average
+    assert max(loads) <= sum(loads) / used + max(weight.values())
+
+
+def test_persistent_schedule_refusals(lib):
+    assert _preview(lib, 0, 1, 64, 65536, 1, 152)[0] == -1      # 64 heads x 256 pairs > 4096 items
+    assert _preview(lib, 2, 1, 1, 128, 1, 152)[0] == -1         # no such kernel
+    assert _preview(lib, 0, 1, 1, 0, 1, 152)[0] == -1           # empty problem
+    off = (ctypes.c_ushort * 153)()
+    items = (ctypes.c_uint * 4)()
+    assert lib.fa_schedule_preview(1, 2, 32, 4096, 1, 152, off, items, 4) == -2
