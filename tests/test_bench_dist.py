@@ -47,3 +47,20 @@ def test_replicas_take_the_slowest_rank():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert results == [(0, 2, 20.0), (1, 2, 20.0)]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference times the oracle on the host and prints one JSON line
+    carrying the metric, the oracle as its cpu_baseline and a copy-free e2e."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["warmup"] >= 3 and d["steps"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
