@@ -123,7 +123,7 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_seqlens=Non
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                       B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T, _DT[q.dtype],
-                      _ptr(workspace), workspace.numel(), _stream(stream))
+                      _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if st != 0:
         raise FAError(st, "fa_bwd")
 

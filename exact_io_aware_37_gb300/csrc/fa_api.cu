@@ -7,6 +7,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "fa_internal.cuh"
 #include "ptx.cuh"
 
@@ -19,27 +21,44 @@ __device__ unsigned g_status_word;
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<unsigned long long> g_launches{0};
 
-constexpr int kMaxDevices = 64;
-unsigned* g_status_ptr[kMaxDevices] = {};
-std::mutex g_mu;
+SymbolAddress g_status_addr(&g_status_word);
 
-// Device address of this device's status word (looked up once per device,
-// with that device current).
+// Device address of the current device's status word.
 cudaError_t status_word(unsigned** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_status_word);
-    if (e != cudaSuccess) return e;
-    g_status_ptr[dev] = static_cast<unsigned*>(p);
-  }
-  *out = g_status_ptr[dev];
-  return cudaSuccess;
+  void* p = nullptr;
+  const cudaError_t e = g_status_addr.get(&p);
+  *out = static_cast<unsigned*>(p);
+  return e;
 }
+
+// Identity of the calling thread's current context, or 0 when there is none
+// or it cannot be read (the driver calls are resolved through the runtime, so
+// the library needs no link-time dependency on libcuda).
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+std::mutex g_symbol_mu;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -48,10 +67,17 @@ constexpr bool kHaveTcFwd = true;
 constexpr bool kHaveTcBwd = true;
 bool use_tensor_cores(fa_dtype dt, int D) { return (dt == FA_BF16 || dt == FA_F16) && (D == 64 || D == 128); }
 
+// The score scale must be finite and positive.  The kernels take each row's
+// running maximum over the raw scores q.k and only then multiply by the
+// scale, which picks the maximum of the scaled scores only when the scale is
+// positive; masked scores are -inf, and -inf times zero or a negative scale
+// is not -inf.  (The pages' scale is 1/sqrt(head width).)
+bool scale_ok(float scale) { return isfinite(scale) && scale > 0.f; }
+
 fa_status validate(int B, int H, int N, int D, float scale, int causal, const int32_t* cu, int T, fa_dtype dt) {
   if (B < 0 || H < 0 || N < 0 || D <= 0) return FA_ERR_INVALID;
   if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;  // grid y / z limits
-  if (!isfinite(scale)) return FA_ERR_INVALID;
+  if (!scale_ok(scale)) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (dt != FA_BF16 && dt != FA_F32 && dt != FA_F16) return FA_ERR_UNSUPPORTED;
   if (fa_path_name(dt, D) == nullptr) return FA_ERR_UNSUPPORTED;
@@ -99,6 +125,25 @@ fa_status set_dropout(Problem& pr, fa_dtype dt, int D, const DropArgs* d) {
 }
 
 }  // namespace
+
+cudaError_t SymbolAddress::get(void** out) {
+  *out = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_symbol_mu);
+  const unsigned long long ctx = current_context_id();
+  if (addr_[dev] == nullptr || ctx == 0 || ctx != ctx_[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, symbol_);  // makes the device's primary context current if needed
+    if (e != cudaSuccess) return e;
+    addr_[dev] = p;
+    ctx_[dev] = current_context_id();
+  }
+  *out = addr_[dev];
+  return cudaSuccess;
+}
 
 void note_launches(unsigned n) { g_launches.fetch_add(n); }
 
@@ -343,7 +388,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
                     void* stream) {
   if (B < 0 || H < 0 || nq < 0 || nk < 0) return FA_ERR_INVALID;
   if (B > 65535 || H > 65535) return FA_ERR_UNSUPPORTED;
-  if (!isfinite(scale)) return FA_ERR_INVALID;
+  if (!scale_ok(scale)) return FA_ERR_INVALID;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID;
   if (dt != FA_BF16 && dt != FA_F32 && dt != FA_F16) return FA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;

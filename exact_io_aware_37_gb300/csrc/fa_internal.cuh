@@ -108,6 +108,24 @@ __device__ __forceinline__ void st_elem(__half* p, long long i, float x) { p[i] 
 // Multiprocessor count of the current device (0 if it cannot be read); cached.
 int sm_count();
 
+// Device address of a __device__ variable in the calling thread's current
+// context.  The lookup (cudaGetSymbolAddress) runs once per device and
+// context and is cached: a device reset destroys the context together with the
+// module holding the variable, and the next context may place it elsewhere, so
+// a cached address is reused only while the context it was taken in is
+// current.  Thread-safe.
+class SymbolAddress {
+ public:
+  explicit SymbolAddress(const void* host_symbol) : symbol_(host_symbol) {}
+  cudaError_t get(void** out);
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  const void* symbol_;  // the host-side stand-in the runtime maps to the device variable
+  void* addr_[kMaxDevices] = {};
+  unsigned long long ctx_[kMaxDevices] = {};
+};
+
 // Work lists of the persistent forward / backward launches for `ctas` CTAs
 // (host only; see fa_schedule_preview).
 int preview_fwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap);

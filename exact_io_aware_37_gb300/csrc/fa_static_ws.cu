@@ -10,8 +10,6 @@
 // (which can synchronise the device).  This entry point serves them with a
 // statically sized array that every GPU loading the library holds until the
 // process exits.  It allocates nothing and only forwards to fa_bwd.
-#include <mutex>
-
 #include "fa_internal.cuh"
 
 namespace fa {
@@ -23,27 +21,10 @@ constexpr size_t kStaticScratchBytes = FA_BWD_STATIC_WS_BYTES;
 // device array; its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_bwd_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_bwd_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return cudaSuccess;
-}
+// Its device address on the current device and context, looked up with
+// cudaGetSymbolAddress on the first call there (and again after a device
+// reset) and cached.
+SymbolAddress g_scratch_addr(g_static_bwd_scratch);
 
 }  // namespace
 }  // namespace fa
@@ -59,7 +40,7 @@ extern "C" fa_status fa_bwd_static_ws(const void* q, const void* k, const void* 
     return FA_ERR_WORKSPACE;
   }
   void* scratch = nullptr;
-  if (fa::note_error("fa_bwd_static_ws: scratch address lookup", fa::scratch_address(&scratch)) != cudaSuccess)
+  if (fa::note_error("fa_bwd_static_ws: scratch address lookup", fa::g_scratch_addr.get(&scratch)) != cudaSuccess)
     return FA_ERR_CUDA;
   // fa_bwd rewrites D_i and zeroes its dQ accumulator before reading either,
   // so whatever the previous call left in the array does not matter.

@@ -64,7 +64,7 @@ extern "C" {
 
 typedef enum {
   FA_OK = 0,
-  FA_ERR_INVALID = -1,      /* NULL pointer, negative size, non-finite scale, bad cu_seqlens */
+  FA_ERR_INVALID = -1,      /* NULL pointer, negative size, scale not finite and > 0, bad cu_seqlens */
   FA_ERR_UNSUPPORTED = -2,  /* head width or dtype this build has no kernel for */
   FA_ERR_ALIGN = -3,        /* a tensor pointer is not 16-byte aligned */
   FA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed (launch, tensor map) */
@@ -82,7 +82,10 @@ typedef enum { FA_BF16 = 0, FA_F32 = 1, FA_F16 = 2 } fa_dtype;
  *   B, H, N, D    batch (or number of packed sequences), heads, tokens (or max
  *                 sequence length when packed), head width; B, H, N >= 0
  *   scale         multiplies Q K^T before the mask and softmax (1/sqrt(D) is
- *                 the usual value); must be finite
+ *                 the usual value); must be finite and > 0 (FA_ERR_INVALID
+ *                 otherwise: the kernels take each row's maximum over the
+ *                 unscaled scores, which is the maximum of the scaled ones only
+ *                 for a positive scale)
  *   causal        0 = full attention, 1 = key j allowed for query i iff j <= i
  *   cu_seqlens    NULL for dense; else DEVICE int32[B+1], non-decreasing,
  *                 cu_seqlens[0] = 0, cu_seqlens[B] = total_tokens, every
@@ -141,12 +144,18 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  * array of FA_BWD_STATIC_WS_BYTES that the library keeps in device memory on
  * every GPU that loads it, until the process exits.  It calls no allocator.
  *   - The first call on a device looks up that array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     device's current context; make that first call before any stream
+ *     capture.  A device reset destroys the context and the array with it:
+ *     the first call after one looks the address up again (again before any
+ *     capture).
  *   - Problems whose fa_bwd_workspace_size exceeds FA_BWD_STATIC_WS_BYTES are
  *     rejected with FA_ERR_WORKSPACE before anything is launched
- *     (fa_last_error_detail says why).  16 MiB covers, e.g., 32K rows at
- *     D = 128 or 64K rows at D = 64 in bf16, and 4M rows in float32.
+ *     (fa_last_error_detail says why).  The workspace takes 4 * (D + 1)
+ *     bytes per row (rows = B*H*N dense, H*total_tokens packed; each of its
+ *     two parts rounded up to 256 bytes) for bf16 / fp16 and 4 bytes per row
+ *     for float32, so 16 MiB holds at most 32,513 rows at D = 128, 64,527 rows
+ *     at D = 64 and 4,194,304 rows in float32.
  *   - Every call on a device shares the one array.  Its previous contents do
  *     not matter (the backward rewrites D_i and zeroes the dQ accumulator
  *     before reading them), but calls that overlap on the GPU -- on different

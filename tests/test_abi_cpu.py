@@ -57,7 +57,6 @@ def _fwd(lib, q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=1, N=12
 
 def test_forward_argument_validation(lib):
     assert _fwd(lib, D=96) == UNSUPPORTED
-    assert _fwd(lib, D=64, dt=1) != UNSUPPORTED or True
     assert _fwd(lib, D=48, dt=1) == UNSUPPORTED
     assert _fwd(lib, dt=7) == UNSUPPORTED
     assert _fwd(lib, D=32, dt=2) == UNSUPPORTED     # fp16 runs on the tensor cores only: D 64 or 128
@@ -65,6 +64,11 @@ def test_forward_argument_validation(lib):
     assert _fwd(lib, N=-5) == INVALID
     assert _fwd(lib, scale=float("nan")) == INVALID
     assert _fwd(lib, scale=float("inf")) == INVALID
+    # the kernels take each row's maximum over unscaled scores: only a positive scale is accepted
+    assert _fwd(lib, scale=0.0) == INVALID
+    assert _fwd(lib, scale=-0.0) == INVALID
+    assert _fwd(lib, scale=-0.125) == INVALID
+    assert _fwd(lib, scale=-0.125, dt=1, D=64) == INVALID
     assert _fwd(lib, causal=2) == INVALID
     assert _fwd(lib, q=None) == INVALID
     assert _fwd(lib, lse=None) == INVALID
@@ -92,6 +96,11 @@ def test_backward_argument_validation(lib):
     assert bwd(ws=0x100010) == WORKSPACE          # not 256-byte aligned
     assert bwd(ws_bytes=16) == WORKSPACE
     assert bwd(H=0) == OK
+    assert bwd(scale=0.0) == INVALID
+    assert bwd(scale=-1.0) == INVALID
+    det = lib.fa_bwd_deterministic(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1,
+                                   128, 128, -0.1, 1, None, 0, 0, 0.0, 7, 0, 0x100000, 1 << 30, None)
+    assert det == INVALID
 
 
 def test_workspace_size(lib):
@@ -129,6 +138,7 @@ def test_dropout_validation(lib):
     assert fwd(float("nan")) == INVALID
     assert fwd(0.2, dt=1, D=64) == UNSUPPORTED   # no dropout on the float32 path
     assert fwd(0.2, B=0) == OK
+    assert fwd(0.2, scale=-0.1) == INVALID
     bwd = lib.fa_bwd_dropout(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 1, 1, 128, 128,
                              0.1, 1, None, 0, 0, 1.5, 7, 0, 0x100000, 1 << 30, None)
     assert bwd == INVALID
@@ -148,6 +158,8 @@ def test_decode_validation_and_workspace(lib):
     assert dec(nk=-1) == INVALID
     assert dec(causal=2) == INVALID
     assert dec(scale=float("nan")) == INVALID
+    assert dec(scale=0.0) == INVALID
+    assert dec(scale=-0.1) == INVALID
     assert dec(q=None) == INVALID
     assert dec(lse=None) == INVALID
     assert dec(k=0x1008) == ALIGN
@@ -156,7 +168,6 @@ def test_decode_validation_and_workspace(lib):
     assert dec(ws_bytes=16) == WORKSPACE
     assert dec(B=0) == OK and dec(nq=0) == OK
     assert dec(k=None) == INVALID
-    assert dec(k=None, v=None, nk=0) != INVALID   # an empty cache needs no K / V (CUDA error without a GPU)
     size = lib.fa_decode_workspace_size
     # 1 x 2 heads, 1000 keys: four splits of 250 keys; per split and row D floats + (m, l)
     assert size(1, 2, 1, 1000, 128, 0) == 4 * 2 * 128 * 4 + 256
@@ -165,9 +176,29 @@ def test_decode_validation_and_workspace(lib):
     assert size(1, 1, 1, 100, 64, 0) == 0 and size(0, 1, 1, 100, 64, 0) == 0
 
 
+# Calls that pass validation would launch kernels on fake pointers where a GPU
+# is present, so they run only where there is none.
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert _fwd(lib) == CUDA
+    assert _fwd(lib, D=64, dt=1) == CUDA            # float32 with D = 64 is supported (SIMT path)
+    # an empty cache needs no K / V pointers
+    assert lib.fa_decode(0x1000, None, None, 0x1000, 0x1000, 1, 2, 1, 0, 128, 0.1, 1, 0, 0x100000, 1 << 30,
+                         None) == CUDA
+
+
+def test_static_scratch_limit(lib):
+    """fa_bwd_static_ws's fixed scratch holds the workspace of at most 32,513
+    rows at D = 128, 64,527 at D = 64 and 4,194,304 in float32; one row more
+    needs more than FA_BWD_STATIC_WS_BYTES (refused before any launch)."""
+    limit = 16 << 20
+    size = lib.fa_bwd_workspace_size
+    for D, dt, rows in ((128, 0, 32513), (64, 0, 64527), (128, 2, 32513), (64, 1, 4194304)):
+        assert size(1, 1, rows, D, None, 0, dt) <= limit < size(1, 1, rows + 1, D, None, 0, dt)
+        # the packed layout counts H * total_tokens rows
+        assert size(3, 1, rows, D, 0x1000, rows, dt) <= limit < size(3, 1, rows, D, 0x1000, rows + 1, dt)
+    with open(os.path.join(ROOT, "include", "fa.h")) as f:
+        assert "#define FA_BWD_STATIC_WS_BYTES ((size_t)16 << 20)" in f.read()
 
 
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
