@@ -23,6 +23,10 @@ none of them re-types the formula below):
   backward_head                  central finite differences of <dO, O>,
                                  torch autograd (float64, CPU), sum_j dK_j = 0,
                                  sum_j dV_j = sum_i dO_i.
+    (o_stored argument)          with the exact O it gives the default result;
+                                 dV never changes; dQ and dK move by the
+                                 closed-form first-order term of a shift of D
+                                 (exact, dS being linear in D).
   forward / backward             reduce to the *_head functions per (b, h);
                                  pinned through them plus a layout test.
   forward_varlen/backward_varlen equal to running each packed sequence as its
@@ -109,7 +113,7 @@ def forward_head(q, k, v, scale, causal):
     return O, L
 
 
-def backward_head(q, k, v, do, scale, causal):
+def backward_head(q, k, v, do, scale, causal, o_stored=None):
     """Analytic gradients of attention for one head given upstream dO.
 
     The pages state only that the backward pass rebuilds each weight as
@@ -122,6 +126,11 @@ def backward_head(q, k, v, do, scale, causal):
         dS = P o (dP - D)          (softmax Jacobian, row by row)
         dQ = scale * dS K
         dK = scale * dS^T Q
+    ``o_stored``: a one-pass backward cannot form sum_j P_ij dP_ij before it
+    needs dS, so it uses the identity sum_j P_ij (dO_i . v_j) = dO_i . O_i and
+    takes D_i = rowsum(dO o O) over the forward output as stored (rounded to
+    the output dtype).  Passing that array here evaluates the same formula;
+    None (the default) keeps the exact D.  dV does not involve D.
     Returns (dQ, dK, dV, D).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -130,7 +139,7 @@ def backward_head(q, k, v, do, scale, causal):
     # P_ij = exp(s_ij - L_i): the same weights section 7 reconstructs.
     dV = P.T @ do
     dP = do @ v.T
-    D = (P * dP).sum(axis=1)
+    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)
     dS = P * (dP - D[:, None])
     dQ = scale * (dS @ k)
     dK = scale * (dS.T @ q)
@@ -157,8 +166,9 @@ def forward(q, k, v, scale, causal):
     return O, L
 
 
-def backward(q, k, v, do, scale, causal):
-    """Dense [B, H, N, D] backward: (dQ, dK, dV, D)."""
+def backward(q, k, v, do, scale, causal, o_stored=None):
+    """Dense [B, H, N, D] backward: (dQ, dK, dV, D).  ``o_stored`` as for
+    backward_head ([B, H, N, D] or None)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, _ = q.shape
     dQ = np.zeros_like(q)
@@ -168,7 +178,8 @@ def backward(q, k, v, do, scale, causal):
     for b in range(B):
         for h in range(H):
             dQ[b, h], dK[b, h], dV[b, h], Dv[b, h] = backward_head(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal,
+                None if o_stored is None else o_stored[b, h])
     return dQ, dK, dV, Dv
 
 
@@ -229,17 +240,18 @@ def forward_head_dropout(q, k, v, scale, causal, p, keep):
     return (P * keep / (1.0 - p)) @ _f64(v), L
 
 
-def backward_head_dropout(q, k, v, do, scale, causal, p, keep):
+def backward_head_dropout(q, k, v, do, scale, causal, p, keep, o_stored=None):
     """Gradients with dropout.  With M = Z / (1 - p) and P~ = P o M:
     dV = P~^T dO, dP = (dO V^T) o M, D_i = sum_j P_ij dP_ij (= dO_i . O_i),
-    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q."""
+    dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.  ``o_stored``
+    (the dropped output as stored) replaces D as in backward_head."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     s = score_matrix(q, k, scale, causal)
     P, _, _, _ = _softmax_rows(s)
     M = keep / (1.0 - p)
     dV = (P * M).T @ do
     dP = (do @ v.T) * M
-    D = (P * dP).sum(axis=1)
+    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)
     dS = P * (dP - D[:, None])
     return scale * (dS @ k), scale * (dS.T @ q), dV, D
 
@@ -257,7 +269,7 @@ def forward_dropout(q, k, v, scale, causal, p, seed, offset):
     return O, L
 
 
-def backward_dropout(q, k, v, do, scale, causal, p, seed, offset):
+def backward_dropout(q, k, v, do, scale, causal, p, seed, offset, o_stored=None):
     """Dense [B, H, N, D] backward with dropout: (dQ, dK, dV, D)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, _ = q.shape
@@ -267,7 +279,8 @@ def backward_dropout(q, k, v, do, scale, causal, p, seed, offset):
         for h in range(H):
             keep = dropout_keep(N, N, b * H + h, p, seed, offset)
             dQ[b, h], dK[b, h], dV[b, h], Dv[b, h] = backward_head_dropout(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, p, keep)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, p, keep,
+                None if o_stored is None else o_stored[b, h])
     return dQ, dK, dV, Dv
 
 
@@ -340,8 +353,9 @@ def forward_varlen(q, k, v, cu_seqlens, scale, causal, heads=None):
     return O, L
 
 
-def backward_varlen(q, k, v, do, cu_seqlens, scale, causal, heads=None):
-    """Packed [H, T, D] backward: (dQ, dK, dV, D); each sequence alone."""
+def backward_varlen(q, k, v, do, cu_seqlens, scale, causal, heads=None, o_stored=None):
+    """Packed [H, T, D] backward: (dQ, dK, dV, D); each sequence alone.
+    ``o_stored`` ([H, T, D] or None) as for backward_head."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     H, T, _ = q.shape
     dQ = np.full(q.shape, np.nan)
@@ -352,7 +366,8 @@ def backward_varlen(q, k, v, do, cu_seqlens, scale, causal, heads=None):
         for a, b in _segments(cu_seqlens):
             if b > a:
                 dQ[h, a:b], dK[h, a:b], dV[h, a:b], Dv[h, a:b] = backward_head(
-                    q[h, a:b], k[h, a:b], v[h, a:b], do[h, a:b], scale, causal)
+                    q[h, a:b], k[h, a:b], v[h, a:b], do[h, a:b], scale, causal,
+                    None if o_stored is None else o_stored[h, a:b])
     return dQ, dK, dV, Dv
 
 

@@ -324,6 +324,62 @@ def check_dropout(impl):
                 assert abs((fp - fm) / (2 * h) - grad[i, j]) < 1e-6
 
 
+def check_stored_o(impl):
+    """The o_stored form of the backward: D_i = rowsum(dO o O) over a given
+    output.  With the exact O from forward_head it equals the default backward
+    (the identity sum_j P_ij dP_ij = dO_i . O_i).  With O + E, dV is unchanged
+    and, dS being linear in D, dQ and dK move by exactly
+    -scale diag(delta) P K and -scale P^T diag(delta) Q, delta = rowsum(dO o E),
+    with P read off forward_head with V = I.  The dense, packed and dropout
+    forms pass the array through head by head."""
+    r = _rng(31)
+    for n, d, causal in ((9, 4, False), (12, 5, True)):
+        q, k, v, do = r.standard_normal((4, n, d))
+        scale = 0.4
+        O, _ = impl.forward_head(q, k, v, scale, causal)
+        ref = impl.backward_head(q, k, v, do, scale, causal)
+        same = impl.backward_head(q, k, v, do, scale, causal, O)
+        for a, b in zip(ref, same):
+            np.testing.assert_allclose(b, a, atol=1e-12)
+        E = 1e-3 * r.standard_normal((n, d))
+        dQ, dK, dV, D = impl.backward_head(q, k, v, do, scale, causal, O + E)
+        P, _ = impl.forward_head(q, k, np.eye(n), scale, causal)
+        delta = (do * E).sum(1)
+        np.testing.assert_allclose(D - ref[3], delta, atol=1e-13)
+        assert np.array_equal(dV, ref[2])
+        np.testing.assert_allclose(dQ - ref[0], -scale * delta[:, None] * (P @ k), atol=1e-12)
+        np.testing.assert_allclose(dK - ref[1], -scale * P.T @ (delta[:, None] * q), atol=1e-12)
+        # dropout form with every weight kept and p = 0: the plain form
+        keep = np.ones((n, n), dtype=bool)
+        got = impl.backward_head_dropout(q, k, v, do, scale, causal, 0.0, keep, O + E)
+        for a, b in zip((dQ, dK, dV, D), got):
+            np.testing.assert_allclose(b, a, atol=1e-12)
+    # batched forms hand each head its own slice of o_stored
+    B, H, n, d = 2, 3, 7, 4
+    q, k, v, do = r.standard_normal((4, B, H, n, d))
+    Ost = r.standard_normal((B, H, n, d))
+    dQ, dK, dV, D = impl.backward(q, k, v, do, 0.3, True, Ost)
+    for b in range(B):
+        for h in range(H):
+            one = impl.backward_head(q[b, h], k[b, h], v[b, h], do[b, h], 0.3, True, Ost[b, h])
+            for a, x in zip(one, (dQ[b, h], dK[b, h], dV[b, h], D[b, h])):
+                np.testing.assert_allclose(x, a, atol=1e-12)
+    cu = np.array([0, 3, 3, 7])
+    qp, kp, vp, dop, Op = (x.reshape(B * H, n, d)[:H] for x in (q, k, v, do, Ost))
+    dQ, dK, dV, D = impl.backward_varlen(qp, kp, vp, dop, cu, 0.3, True, o_stored=Op)
+    for h in range(H):
+        for a0, a1 in ((0, 3), (3, 7)):
+            one = impl.backward_head(qp[h, a0:a1], kp[h, a0:a1], vp[h, a0:a1], dop[h, a0:a1], 0.3, True,
+                                     Op[h, a0:a1])
+            for a, x in zip(one, (dQ[h, a0:a1], dK[h, a0:a1], dV[h, a0:a1], D[h, a0:a1])):
+                np.testing.assert_allclose(x, a, atol=1e-12)
+    keep = impl.dropout_keep(n, n, 4, 0.3, 99, 1)
+    dQ, dK, dV, D = impl.backward_dropout(q, k, v, do, 0.3, False, 0.3, 99, 1, Ost)
+    one = impl.backward_head_dropout(q[1, 1], k[1, 1], v[1, 1], do[1, 1], 0.3, False, 0.3, keep, Ost[1, 1])
+    for a, x in zip(one, (dQ[1, 1], dK[1, 1], dV[1, 1], D[1, 1])):
+        np.testing.assert_allclose(x, a, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_split_tile_example,
     check_zero_query,
@@ -337,4 +393,5 @@ ALL_CHECKS = [
     check_cached_decoding,
     check_philox_known_answers,
     check_dropout,
+    check_stored_o,
 ]

@@ -47,10 +47,28 @@ MUTANTS = {
                          "    dK = scale * (dS.T @ k)\n    return dQ, dK, dV, D"),
     "dQ_missing_scale": ("    dQ = scale * (dS @ k)\n    dK",
                          "    dQ = (dS @ k)\n    dK"),
-    "D_missing_P": ("    D = (P * dP).sum(axis=1)\n    dS = P * (dP - D[:, None])\n    dQ = scale",
-                    "    D = dP.sum(axis=1)\n    dS = P * (dP - D[:, None])\n    dQ = scale"),
-    "dropout_D_missing_P": ("    D = (P * dP).sum(axis=1)\n    dS = P * (dP - D[:, None])\n    return scale",
-                            "    D = dP.sum(axis=1)\n    dS = P * (dP - D[:, None])\n    return scale"),
+    "D_missing_P": ("    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                    "    dS = P * (dP - D[:, None])\n    dQ = scale",
+                    "    D = dP.sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                    "    dS = P * (dP - D[:, None])\n    dQ = scale"),
+    "stored_o_ignored": ("    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                         "    dS = P * (dP - D[:, None])\n    dQ = scale",
+                         "    D = (P * dP).sum(axis=1)\n    dS = P * (dP - D[:, None])\n    dQ = scale"),
+    "stored_o_wrong_operand": ("    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                               "    dS = P * (dP - D[:, None])\n    dQ = scale",
+                               "    D = (P * dP).sum(axis=1) if o_stored is None else (v * _f64(o_stored)).sum(axis=1)\n"
+                               "    dS = P * (dP - D[:, None])\n    dQ = scale"),
+    "stored_o_wrong_head": ("                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal,\n"
+                            "                None if o_stored is None else o_stored[b, h])",
+                            "                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal,\n"
+                            "                None if o_stored is None else o_stored[h % B, b % H])"),
+    "dropout_D_missing_P": ("    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                            "    dS = P * (dP - D[:, None])\n    return scale",
+                            "    D = dP.sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                            "    dS = P * (dP - D[:, None])\n    return scale"),
+    "dropout_stored_o_ignored": ("    D = (P * dP).sum(axis=1) if o_stored is None else (do * _f64(o_stored)).sum(axis=1)\n"
+                                 "    dS = P * (dP - D[:, None])\n    return scale",
+                                 "    D = (P * dP).sum(axis=1)\n    dS = P * (dP - D[:, None])\n    return scale"),
     "dV_missing_transpose": ("    dV = P.T @ do\n    dP = do @ v.T",
                              "    dV = P @ do\n    dP = do @ v.T"),
     "cached_mask_top_left": ("        s = np.where(j <= i + (nk - nq), s, -np.inf)",
