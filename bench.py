@@ -69,22 +69,73 @@ def hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 50 ms) taken while the timed region runs."""
+    """SM clock, power and clock-event reasons sampled while the timed region
+    runs: read in-process through NVML (read-only queries, every ~1 ms, so a
+    timed region of a few milliseconds still gets many samples); nvidia-smi
+    at 50 ms where the NVML library cannot be loaded."""
 
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_s=0.0002):
         self.index = index
-        self.proc = None
+        self.period_s = period_s
+        self.samples = []  # (sm_mhz, max_mhz, power_w, reason_bits)
         self.lines = []
+        self.source = None
+        self.proc = None
+        self.thread = None
+        self._stop = threading.Event()
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.index)
+        bus = None
+        if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0".encode()
+        if bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        return nv, h
+
+    def _poll_nvml(self, nv, h):
+        import ctypes
+        sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        max_ok = nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0  # fixed: read once
+        n = 0
+        while not self._stop.is_set():
+            ok = max_ok and nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0      # NVML_CLOCK_SM
+            ok = ok and reasons_fn(h, ctypes.byref(rs)) == 0
+            power = n % 8 == 0 and nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0
+            if ok:
+                self.samples.append((sm.value, mx.value, pw.value / 1e3 if power else None, rs.value))
+            n += 1
+            self._stop.wait(self.period_s)
 
     def __enter__(self):
+        try:
+            nv, h = self._nvml_handle()
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, args=(nv, h), daemon=True)
+            self.thread.start()
+            return self
+        except (OSError, AttributeError, RuntimeError):
+            pass
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, ValueError):
@@ -96,15 +147,24 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
+        for s_mhz, m_mhz, p_w, bits in self.samples:
+            sm.append(float(s_mhz))
+            mx.append(float(m_mhz))
+            if p_w is not None:
+                pw.append(p_w)
+            reasons.update(name for bit, name in self.REASONS.items() if bits & bit)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [x.strip() for x in line.split(",")]
@@ -113,15 +173,17 @@ class ClockSampler:
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
             except ValueError:
                 continue
             for name, val in zip(names, parts[3:7]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_min_mhz": min(sm),
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw) if pw else None,
+                "source": self.source}
 
 
 def dist_setup(n_gpus):
@@ -229,9 +291,14 @@ def main():
                     help="attention dropout probability for the train workload (fa_fwd_dropout / fa_bwd_dropout)")
     ap.add_argument("--deterministic", action="store_true",
                     help="train workload with fa_bwd_deterministic (dQ without atomics)")
-    ap.add_argument("--workload", choices=["train", "decode"], default="train",
-                    help="train: causal fwd+bwd at B2 H32 N4096 D128 (the default); "
-                         "decode: one cached decoding step, B16 H32, 1 query, 8192 keys, D128")
+    ap.add_argument("--probe", choices=["ex2"], default=None,
+                    help="ex2: measure the special-function units' ex2.approx rate and print, for the train "
+                         "workload's kernels, the exponential-bound time beside the tensor-core-bound time")
+    ap.add_argument("--workload", choices=["train", "decode"] + sorted(CONFIG_WORKLOADS), default="train",
+                    help="train: causal fwd+bwd at B2 H32 N4096 D128 (the default, with the e2e and CPU legs); "
+                         "decode: one cached decoding step, B16 H32, 1 query, 8192 keys, D128; "
+                         "mid / long / long_nc / varlen / window: fwd+bwd of the other configurations "
+                         "(device-resident inputs, kernel timings and roofline only)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -246,8 +313,14 @@ def main():
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.probe == "ex2":
+        probe_ex2(fa, synth, local, device)
+        return
     if args.workload == "decode":
         bench_decode(fa, synth, args, dist, rank, world, local, device)
+        return
+    if args.workload in CONFIG_WORKLOADS:
+        bench_config(fa, synth, args, dist, rank, world, local, device)
         return
     cfg = dict(synth.WORKLOADS[WORKLOAD], dtype=args.dtype)
     q_h, k_h, v_h, do_h = synth.make_dense(cfg)
@@ -356,6 +429,138 @@ def main():
     barrier(dist)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def probe_ex2(fa, synth, local, device):
+    """Measured ex2.approx rate (exponentials per clock per SM) and, for each
+    tensor-core kernel of the train workload, the time its exponentials take
+    at that rate beside the time its products take at the tensor core's
+    nominal bf16 rate (8192 flop per clock per SM) and at the measured peak."""
+    with ClockSampler(local) as clocks:
+        rates = [fa.fa_probe_ex2_rate(iters=1 << 14) for _ in range(5)]
+    rate = statistics.median(rates)
+    cfg = synth.WORKLOADS[WORKLOAD]
+    B, H, N, D = cfg["B"], cfg["H"], cfg["N"], cfg["D"]
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = 2070.0
+    peak_tf, _, peak_kind = peaks()
+    exps = B * H * N * N / (2 if CAUSAL else 1)   # one exponential per allowed score, each pass
+    f_fwd = flops_fwd(B, H, N, D, CAUSAL)
+    kernels = {}
+    for name, flops in (("tc_fwd_kernel", f_fwd), ("tc_bwd128_kernel", 2.5 * f_fwd)):
+        kernels[name] = {
+            "exponentials": exps,
+            "ex2_bound_us": 1e6 * exps / (rate * sms * mhz * 1e6),
+            "tensor_bound_us_nominal": 1e6 * flops / (8192.0 * sms * mhz * 1e6),
+            "tensor_bound_us_measured_peak": 1e6 * flops / (peak_tf * 1e12),
+        }
+    line = {"probe": "ex2.approx.f32 rate", "ex2_per_clk_per_sm": rate, "samples": rates, "sms": sms,
+            "clock_mhz_for_times": mhz, "workload": f"{WORKLOAD} causal", "kernels": kernels,
+            "peak_kind": f"bf16 dense burst, {peak_kind}", "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+
+
+# The other configurations: synth workload name and whether the mask is on.
+CONFIG_WORKLOADS = {
+    "mid": ("mid_b4h16n1024d64", True),
+    "long": ("long_b2h32n4096d128", True),
+    "long_nc": ("long_b2h32n4096d128", False),
+    "varlen": ("varlen16_h32d128", True),
+    "window": ("window_b1h32n32768d128", True),
+}
+
+
+def bench_config(fa, synth, args, dist, rank, world, local, device):
+    """fwd+bwd TFLOP/s of one configuration with inputs resident on the
+    device: fa_fwd then fa_bwd per step, each timed with CUDA events on the
+    launching stream, the main backward kernel timed alone by the events the
+    library records around it.  Packed input counts sum_s 4 H n_s^2 D (half
+    with the mask) forward FLOPs."""
+    name, causal = CONFIG_WORKLOADS[args.workload]
+    cfg = dict(synth.WORKLOADS[name], dtype=args.dtype)
+    cu = max_seqlen = None
+    if "n_seqs" in cfg:
+        q_h, k_h, v_h, do_h, cu_h, lengths = synth.make_varlen(cfg)
+        H, T, D = q_h.shape
+        f_fwd = sum(flops_fwd(1, H, int(n), D, causal) for n in lengths.tolist())
+        cu, max_seqlen = cu_h.to(device), int(lengths.max())
+        shape_cfg = {"H": H, "T": T, "D": D, "n_seqs": len(lengths), "max_seqlen": max_seqlen}
+    else:
+        q_h, k_h, v_h, do_h = synth.make_dense(cfg)
+        B, H, N, D = q_h.shape
+        f_fwd = flops_fwd(B, H, N, D, causal)
+        shape_cfg = {"B": B, "H": H, "N": N, "D": D}
+    scale = 1.0 / D ** 0.5
+    q, k, v, do = (x.to(device) for x in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(q, cu, max_seqlen), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fwd():
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, cu, max_seqlen, stream=stream)
+
+    def bwd():
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, cu, max_seqlen, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in ev:
+        e[3].record(stream)
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    launches0 = fa.fa_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for st in range(args.steps):
+            ev[st][0].record(stream)
+            fwd()
+            ev[st][1].record(stream)
+            fa.fa_bwd_time_main_kernel(ev[st][3], ev[st][4])
+            bwd()
+            ev[st][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    launches = fa.fa_launch_count() - launches0
+    assert fa.fa_get_last_device_error() == 0
+    ms_step = max_over_ranks(dist, t0.elapsed_time(t1), device) / args.steps
+    ms_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    ms_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms_main = statistics.mean(e[3].elapsed_time(e[4]) for e in ev)
+    peak_tf, _, peak_kind = peaks()
+    value = world * 3.5 * f_fwd / (ms_step * 1e-3) / 1e12
+    bwd_main_tf = 2.5 * f_fwd / (ms_main * 1e-3) / 1e12
+    kernel = "tc_bwd128_kernel" if D == 128 else "tc_bwd_kernel<64>"
+    if rank != 0:
+        return
+    line = {
+        "metric": f"attention fwd & fwd+bwd TFLOP/s ({args.dtype}, {'causal' if causal else 'non-causal'}) "
+                  "and % of GB300 BF16 tensor peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": args.dtype, "data": "synthetic",
+        "config": dict({"workload": f"{name} {'causal' if causal else 'non-causal'}", "causal": causal,
+                        "kernel_path": fa.fa_path_name(q.dtype, D),
+                        "l2": f"inputs {4 * q.numel() * q.element_size() / 2**20:.0f} MiB; no flush",
+                        "parallelism": f"replicas x{world}"}, **shape_cfg),
+        "fwd_tflops": f_fwd / (ms_fwd * 1e-3) / 1e12, "bwd_tflops": 2.5 * f_fwd / (ms_bwd * 1e-3) / 1e12,
+        "fwd_frac_of_peak": f_fwd / (ms_fwd * 1e-3) / 1e12 / peak_tf, "fwdbwd_frac_of_peak": value / world / peak_tf,
+        "ms_fwd": ms_fwd, "ms_bwd": ms_bwd, "ms_bwd_main_kernel": ms_main,
+        "roofline": {"bound": "tensor", "achieved": bwd_main_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": bwd_main_tf / peak_tf, "traffic": None, "kernel": kernel,
+                     "peak_kind": f"bf16 dense burst, {peak_kind}"},
+        "gpu_launches": launches, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
 
 
 DECODE_WORKLOAD = "decode_b16h32q1k8192d128"

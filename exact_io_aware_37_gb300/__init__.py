@@ -20,7 +20,7 @@ from ._lib import FA_BF16, FA_F16, FA_F32, FAError, lib, library_path  # noqa: F
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
            "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
            "fa_decode", "fa_decode_workspace_size", "decode", "fa_fwd_dropout", "fa_bwd_dropout",
-           "fa_bwd_deterministic", "FAError"]
+           "fa_bwd_deterministic", "fa_probe_ex2_rate", "FAError"]
 
 _DT = {torch.bfloat16: FA_BF16, torch.float32: FA_F32, torch.float16: FA_F16}
 
@@ -80,6 +80,17 @@ def fa_bwd_time_main_kernel(start_event, stop_event):
     """Have the next fa_bwd on this thread record the two torch.cuda.Events
     (already recorded once, so they exist) around its main gradient kernel."""
     lib().fa_bwd_time_main_kernel(start_event.cuda_event, stop_event.cuda_event)
+
+
+def fa_probe_ex2_rate(iters=4096, stream=None):
+    """Measured ex2.approx throughput, exponentials per clock per SM (see
+    fa_probe_ex2_rate in include/fa.h).  Synchronises the stream."""
+    import ctypes
+    out = ctypes.c_double(0.0)
+    st = lib().fa_probe_ex2_rate(int(iters), ctypes.byref(out), _stream(stream))
+    if st != 0:
+        raise FAError(st, "fa_probe_ex2_rate")
+    return out.value
 
 
 def fa_set_wait_limit_ns(limit_ns):

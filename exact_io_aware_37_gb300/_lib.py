@@ -29,7 +29,7 @@ SIGNATURES = {
     "fa_selftest_wait_timeout": (_int, [_vp]),
     "fa_path_name": (_c.c_char_p, [_int, _int]),
     "fa_launch_count": (_c.c_ulonglong, []),
-    "fa_schedule_preview": (_int, [_int, _int, _int, _int, _int, _int, _vp, _vp, _int]),
+    "fa_schedule_preview": (_int, [_int, _vp, _int, _int, _int, _int, _int, _vp, _vp, _int, _vp]),
     "fa_last_error_detail": (_c.c_char_p, []),
     "fa_bwd_time_main_kernel": (None, [_vp, _vp]),
     "fa_fwd_dropout": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int, _vp, _int, _int, _f,
@@ -39,6 +39,7 @@ SIGNATURES = {
     "fa_bwd_deterministic": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int,
                                     _vp, _int, _int, _f, _c.c_uint64, _c.c_uint32, _vp, _sz, _vp]),
     "fa_decode_workspace_size": (_sz, [_int, _int, _int, _int, _int, _int]),
+    "fa_probe_ex2_rate": (_int, [_int, _c.POINTER(_c.c_double), _vp]),
     "fa_decode": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _f, _int, _int, _vp, _sz, _vp]),
 }
 

@@ -206,19 +206,20 @@ const char* fa_path_name(fa_dtype dt, int D) {
 
 unsigned long long fa_launch_count(void) { return g_launches.load(); }
 
-int fa_schedule_preview(int kernel, int B, int H, int N, int causal, int n_ctas, unsigned short* off,
-                        unsigned int* items, int cap) {
+int fa_schedule_preview(int kernel, const int32_t* cu_seqlens, int B, int H, int N, int causal, int n_ctas,
+                        int* off, unsigned int* items, int cap, int* form) {
   if ((kernel != 0 && kernel != 1) || B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1) || n_ctas <= 0 ||
-      off == nullptr || cap < 0 || (items == nullptr && cap > 0))
+      off == nullptr || form == nullptr || cap < 0 || (items == nullptr && cap > 0))
     return -1;
   fa::Problem p{};
   p.B = B;
   p.H = H;
   p.N = N;
   p.causal = causal;
-  p.cu = nullptr;
-  return kernel == 0 ? fa::preview_fwd_schedule(p, n_ctas, off, items, cap)
-                     : fa::preview_bwd_schedule(p, n_ctas, off, items, cap);
+  p.cu = cu_seqlens;  // only its presence matters to the schedule; the host copy is read below
+  p.T = cu_seqlens ? cu_seqlens[B] : 0;
+  return kernel == 0 ? fa::preview_fwd_schedule(p, cu_seqlens, n_ctas, off, items, cap, form)
+                     : fa::preview_bwd_schedule(p, cu_seqlens, n_ctas, off, items, cap, form);
 }
 
 const char* fa_last_error_detail(void) { return g_detail; }

@@ -127,9 +127,12 @@ class SymbolAddress {
 };
 
 // Work lists of the persistent forward / backward launches for `ctas` CTAs
-// (host only; see fa_schedule_preview).
-int preview_fwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap);
-int preview_bwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap);
+// (host only; see fa_schedule_preview).  cu_host: packed sequence offsets on
+// the host, or nullptr for dense input.  *form: 0 = table, 1 = closed form.
+int preview_fwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int* off, uint32_t* items, int cap,
+                         int* form);
+int preview_bwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int* off, uint32_t* items, int cap,
+                         int* form);
 
 // Counts kernel launches (read by fa_launch_count); every launcher bumps it.
 void note_launches(unsigned n);

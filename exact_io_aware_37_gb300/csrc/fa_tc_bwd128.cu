@@ -5,9 +5,10 @@
 // section 7: every weight is rebuilt as P_ij = exp(s_ij - L_i) from the
 // saved log-sum-exp; dV = P^T dO, dS = P o (dO V^T - D), dK = scale dS^T Q,
 // dQ = scale dS K): a CTA holds one 128-key tile of K and V in shared memory
-// at a time and visits the 128-query tiles that can see it; for dense inputs
-// it is persistent and works through a host-built list of key tiles (see
-// BwdSched).  All five products are
+// at a time and visits the 128-query tiles that can see it; every launch is
+// persistent and each CTA works through a list of key tiles (fa_sched.cuh:
+// a host-built table for dense inputs that fit one, a closed-form list
+// otherwise).  All five products are
 // tcgen05 MMAs with M = N = 128, placed in tensor memory as
 //     [0,128)   S^T = K Q^T, then P^T (bf16) over its columns [0,32) and [64,96)
 //     [128,256) dP^T = V dO^T, then dS^T (bf16) over [128,160) and [192,224),
@@ -45,6 +46,7 @@
 
 #include "fa_dropout.cuh"
 #include "fa_internal.cuh"
+#include "fa_sched.cuh"
 #include "fa_tmap.cuh"
 #include "ptx.cuh"
 
@@ -68,20 +70,26 @@ constexpr int kBwdSupportRegs = 136;
 static_assert(2 * 128 * kBwdComputeRegs + 128 * kBwdSupportRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
 
-// A persistent launch hands each CTA a list of key tiles (b, h, kt) worked
-// out on the host: items in the causal heavy-first order, each given to the
-// CTA with the least work so far (longest processing time first, as the
-// block scheduler would, but without a CTA launch, tensor-memory allocation
-// and pipeline fill per tile: the next tile's loads and first products
-// overlap the previous tile's last reductions and its dK / dV stores).
+// Each CTA of the (always persistent) launch works through a list of key
+// tiles (b, h, kt), so a CTA launch, tensor-memory allocation and pipeline
+// fill are paid once and the next tile's loads and first products overlap
+// the previous tile's last reductions and its dK / dV stores.  Dense inputs
+// of at most kMaxSchedItems tiles get a table worked out on the host: items
+// in the causal heavy-first order inside groups of heads, each given to the
+// CTA with the least work so far (longest processing time first); larger and
+// packed inputs the closed-form list of fa_sched.cuh.
 constexpr int kMaxSchedCtas = 160;
 constexpr int kMaxSchedItems = 4096;
+constexpr int kSchedTable = 0, kSchedClosed = 1;
 
 struct BwdSched {
-  int n_ctas;                         // 0: one key tile per CTA, taken from the grid
-  int n_kt;                           // key tiles per (b, h)
-  uint16_t off[kMaxSchedCtas + 1];    // CTA c works on item[off[c] .. off[c + 1])
-  uint32_t item[kMaxSchedItems];      // (b * H + h) * n_kt + kt
+  int n_ctas;                         // CTAs of the launch
+  int mode;                           // kSchedTable or kSchedClosed
+  int n_kt;                           // table: key tiles per (b, h)
+  uint32_t n_virtual;                 // closed form: (B * H) * ranks
+  uint32_t per, ranks, snake;         // closed form: units per group, key tiles per unit, CTA order
+  uint16_t off[kMaxSchedCtas + 1];    // table: CTA c works on item[off[c] .. off[c + 1])
+  uint32_t item[kMaxSchedItems];      // table: (b * H + h) * n_kt + kt
 };
 
 struct Bwd128Params {
@@ -150,6 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_accfree = bars + 19;  // dK / dV of a key tile read out of TMEM (8 compute warps)
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
+  // step count of key tile ii, in slot ii % 2: written by the producer before
+  // the tile's K / V load is armed on bar_kv, read by the MMA issuer after its
+  // wait on bar_kv (the issuer has no registers to walk the list itself)
+  int* steps_sh = reinterpret_cast<int*>(smem + kMiscOff + 8);
   float* s_l = reinterpret_cast<float*>(smem + kLOff);
   float* s_d = reinterpret_cast<float*>(smem + kDvOff);
 
@@ -159,16 +171,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     int b, h, kt, len, row0, slab, q_first, n_steps;
     long long out_base;
   };
-  const bool persistent = p.sched.n_ctas > 0;
-  int n_items = 1, first_item = 0;
-  if (persistent) {
-    first_item = p.sched.off[blockIdx.x];
-    n_items = p.sched.off[blockIdx.x + 1] - first_item;
-  }
-  auto item_at = [&](int ii) {
-    Item it;
-    if (persistent) {  // dense: every listed tile is in range
-      const uint32_t code = p.sched.item[first_item + ii];
+  const bool table = p.sched.mode == kSchedTable;
+  const int first_item = table ? p.sched.off[blockIdx.x] : 0;
+  const int n_table = table ? p.sched.off[blockIdx.x + 1] - first_item : 0;
+  const ClosedSpec closed{p.sched.n_virtual, (uint32_t)p.B * (uint32_t)p.H, p.sched.per, p.sched.ranks,
+                          (uint32_t)p.sched.n_ctas, p.sched.snake};
+  auto set_steps = [&](Item& it) {
+    const int n_t = (it.len + kTile - 1) / kTile;
+    it.q_first = p.causal ? it.kt : 0;  // earlier query tiles never see these keys
+    it.n_steps = n_t - it.q_first;
+  };
+  // The CTA's next key tile after list position k (k moves past it); false
+  // once the list has ended.  Every role walks the same list.
+  auto next_item = [&](uint32_t& k, Item& it) -> bool {
+    if (table) {  // dense: every listed tile is in range
+      if (k >= (uint32_t)n_table) return false;
+      const uint32_t code = p.sched.item[first_item + (int)k++];
       const int bh = (int)(code / (uint32_t)p.sched.n_kt);
       it.kt = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_kt);
       it.b = bh / p.H;
@@ -177,15 +195,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       it.row0 = 0;
       it.slab = bh;
       it.out_base = (long long)bh * p.N;
-    } else {
-      // causal: early key tiles meet the most query tiles and are handed out first
-      const GridItem g = p.causal ? grouped_heavy_first(kBwdHeadGroup)
-                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
-      it.b = g.b;
-      it.h = g.h;
-      it.kt = g.rank;
+      set_steps(it);
+      return true;
+    }
+    for (;;) {
+      const uint32_t f = closed_item(closed, blockIdx.x, k);
+      if (f >= closed.n_virtual) return false;
+      ++k;
+      uint32_t uu, rr;
+      closed_unit_rank(closed, f, uu, rr);
+      const int r = (int)rr, u = (int)uu;
+      it.b = u / p.H;
+      it.h = u - it.b * p.H;
       if (p.cu != nullptr) {
         const int s0 = p.cu[it.b], s1 = p.cu[it.b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {  // skipped and reported
+          if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
+          continue;
+        }
         it.len = s1 - s0;
         it.row0 = s0;
         it.slab = it.h;
@@ -193,28 +220,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       } else {
         it.len = p.N;
         it.row0 = 0;
-        it.slab = it.b * p.H + it.h;
-        it.out_base = (long long)it.slab * p.N;
+        it.slab = u;
+        it.out_base = (long long)u * p.N;
       }
+      it.kt = bwd_tile_of_rank(it.len, r);
+      if (it.kt < 0) continue;  // the sequence has fewer key tiles
+      set_steps(it);
+      return true;
     }
-    const int n_t = (it.len + kTile - 1) / kTile;
-    it.q_first = p.causal ? it.kt : 0;  // earlier query tiles never see these keys
-    it.n_steps = it.kt < n_t ? n_t - it.q_first : 0;
-    return it;
   };
-  if (!persistent) {
-    if (p.cu != nullptr) {
-      const GridItem g = p.causal ? grouped_heavy_first(kBwdHeadGroup)
-                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
-      const int s0 = p.cu[g.b], s1 = p.cu[g.b + 1];
-      if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
-        if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
-        return;
-      }
-    }
-    if (item_at(0).n_steps <= 0) return;
+  {
+    uint32_t k0 = 0;
+    Item first;
+    if (!next_item(k0, first)) return;  // nothing for this CTA
   }
-  if (n_items <= 0) return;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
@@ -281,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     };
 
     int G = 0;
-    for (int ii = 0; ok && ii < n_items; ++ii) {
-      const Item it = item_at(ii);
+    uint32_t cur = 0;
+    Item it;
+    for (int ii = 0; ok && next_item(cur, it); ++ii) {
       const int b = it.b, h = it.h, len = it.len;
       const int key = it.kt * kTile + j;
       for (int k = 0; ok && k < it.n_steps; ++k) {
@@ -444,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         if (lane == 0) {
           if (ii > 0) good = mbar_wait(bar_itemdone, (ii - 1) & 1, w);
           if (good) {
+            steps_sh[ii & 1] = it.n_steps;  // slot ii - 2 was read before tile ii - 1 began
             mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
             for (int hf = 0; hf < 2; ++hf) {
               tma_load_3d(smem + kKOff + hf * kHalfBytes, &p.tk, bar_kv, hf * 64, it.row0 + it.kt * kTile, it.slab);
@@ -455,8 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         if (good) kv_issued = ii + 1;
         return good != 0;
       };
-      for (int ii = 0; good_all && ii < n_items; ++ii) {
-        const Item it = item_at(ii);
+      uint32_t cur = 0;
+      Item it;
+      for (int ii = 0; good_all && next_item(cur, it); ++ii) {
         // The first tile's K and V go first; a later tile's wait until its first
         // Q, L / D and dO are on their way, which need no more than their buffers.
         if (ii == 0 && !load_kv(it, ii)) break;
@@ -513,8 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         }
         // the next tile's K and V wait for this tile's last products; have them
         // in L2 by then
-        if (lane == 0 && ii + 1 < n_items) {
-          const Item nx = item_at(ii + 1);
+        uint32_t peek = cur;
+        Item nx;
+        if (lane == 0 && next_item(peek, nx)) {
           for (int hf = 0; hf < 2; ++hf) {
             tma_prefetch_l2_3d(&p.tk, hf * 64, nx.row0 + nx.kt * kTile, nx.slab);
             tma_prefetch_l2_3d(&p.tv, hf * 64, nx.row0 + nx.kt * kTile, nx.slab);
@@ -535,8 +558,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       // handed back as soon as it has been read, half 1's after that.
       int G = 0;
       bool good = true;
-      for (int ii = 0; good && ii < n_items; ++ii) {
-        const Item it = item_at(ii);
+      uint32_t cur = 0;
+      Item it;
+      while (good && next_item(cur, it)) {
         for (int kk = 0; good && kk < it.n_steps; ++kk) {
           const int gg = G + kk;
           const int q0 = (it.q_first + kk) * kTile;
@@ -605,20 +629,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       };
       bool ok = true;
       int G = 0;
-      // the step count of each tile, worked out without the rest of its geometry
-      // (this thread has few registers to spare)
-      const int n_steps0 = item_at(0).n_steps;
+      // the CTA's tile count, walked once before the loop (whose registers
+      // the walk would otherwise crowd); each tile's step count comes from
+      // the producer through steps_sh
+      int n_items = 0;
+      {
+        uint32_t cur = 0;
+        Item it;
+        while (next_item(cur, it)) ++n_items;
+      }
       for (int ii = 0; ok && ii < n_items; ++ii) {
-        int n_steps = n_steps0;
-        if (persistent) {
-          const uint32_t code = p.sched.item[first_item + ii];
-          const int kt = (int)(code % (uint32_t)p.sched.n_kt);
-          n_steps = p.causal ? p.sched.n_kt - kt : p.sched.n_kt;
-        }
         // K, V of this tile; S^T and dP^T of its first step.  dP^T goes over the
         // previous tile's last dQ^T, so it waits until that has been read out.
         ok = mbar_wait(bar_kv, ii & 1, w) && mbar_wait(bar_qf + (G & 1), (G >> 1) & 1, w);
         if (!ok) break;
+        const int n_steps = steps_sh[ii & 1];
         tc_fence_after();
         issue_s(G);
         ok = (!kDq || G == 0 || mbar_wait(bar_dqfree, (G - 1) & 1, w)) && mbar_wait(bar_of, G & 1, w);
@@ -724,15 +749,29 @@ int sm_count() {
 // balance of the schedule.
 constexpr int kItemOverheadSteps = 2;
 
-// The work list for at most `ctas_max` CTAs: false (no schedule, one CTA per
-// key tile) for packed inputs, whose tile sizes live on the device, or when
-// the tiles do not fit the parameter block.
+// The work list for at most `ctas_max` CTAs: the table for dense inputs with
+// at most kMaxSchedItems key tiles, the closed-form list otherwise; false when
+// there is nothing to do.
 bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
   sc.n_ctas = 0;
   const int n_kt = (p.N + kTile - 1) / kTile;
   const long long n_bh = (long long)p.B * p.H;
   const long long n = n_bh * n_kt;
-  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || ctas_max <= 0) return false;
+  if (n <= 0 || ctas_max <= 0) return false;
+  sc.n_kt = n_kt;
+  if (p.cu != nullptr || n > kMaxSchedItems) {
+    sc.mode = kSchedClosed;
+    const long long v = n_bh * bwd_ranks(p.N);
+    if (v > (long long)kMaxVirtualItems) return false;
+    sc.n_virtual = (uint32_t)v;
+    sc.per = closed_group_size((uint32_t)n_bh, kBwdHeadGroup);  // a few units at a time stay in L2
+    sc.ranks = (uint32_t)bwd_ranks(p.N);
+    sc.snake = 0;
+    sc.n_ctas = (int)std::min<long long>(v, ctas_max);
+    return true;
+  }
+  sc.mode = kSchedTable;
+  sc.n_virtual = (uint32_t)n;
   const int ctas = (int)std::min<long long>(n, std::min(ctas_max, kMaxSchedCtas));
   // Items in the order the grid used: with the mask, heavy-first inside
   // balanced groups of kBwdHeadGroup heads (the order of grouped_heavy_first).
@@ -773,7 +812,6 @@ bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
   }
   sc.off[ctas] = (uint16_t)at;
   sc.n_ctas = ctas;
-  sc.n_kt = n_kt;
   return true;
 }
 
@@ -785,8 +823,9 @@ bool build_sched(const Problem& p, BwdSched& sc) {
   static long long key[5] = {-1, -1, -1, -1, -1};
   static BwdSched cached;
   const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  if (p.cu != nullptr) return fill_bwd_sched(p, ctas, sc);  // closed form: nothing to cache
   std::lock_guard<std::mutex> lock(mu);
-  if (p.cu == nullptr && std::equal(want, want + 5, key)) {
+  if (std::equal(want, want + 5, key)) {
     sc = cached;
     return true;
   }
@@ -796,15 +835,46 @@ bool build_sched(const Problem& p, BwdSched& sc) {
   return true;
 }
 
-int preview_bwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap) {
+int preview_bwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int* off, uint32_t* items, int cap,
+                         int* form) {
   static BwdSched sc;  // large; previews are a host-side test aid
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (!fill_bwd_sched(p, ctas, sc)) return -1;
-  const int n = sc.off[sc.n_ctas];
-  if (n > cap) return -2;
-  std::copy(sc.off, sc.off + sc.n_ctas + 1, off);
-  std::copy(sc.item, sc.item + n, items);
+  *form = sc.mode;
+  if (sc.mode == kSchedTable) {
+    const int n = sc.off[sc.n_ctas];
+    if (n > cap) return -2;
+    for (int c = 0; c <= sc.n_ctas; ++c) off[c] = sc.off[c];
+    std::copy(sc.item, sc.item + n, items);
+    return n;
+  }
+  // the closed form, walked exactly as the kernel's roles walk it
+  const ClosedSpec closed{sc.n_virtual, (uint32_t)p.B * (uint32_t)p.H, sc.per, sc.ranks, (uint32_t)sc.n_ctas,
+                          sc.snake};
+  const int ranks = bwd_ranks(p.N);
+  int n = 0;
+  for (int c = 0; c < sc.n_ctas; ++c) {
+    off[c] = n;
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t f = closed_item(closed, (uint32_t)c, k);
+      if (f >= closed.n_virtual) break;
+      uint32_t uu, rr;
+      closed_unit_rank(closed, f, uu, rr);
+      const int r = (int)rr, u = (int)uu;
+      int len = p.N;
+      if (cu_host != nullptr) {
+        const int b = u / p.H, s0 = cu_host[b], s1 = cu_host[b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) continue;
+        len = s1 - s0;
+      }
+      const int kt = bwd_tile_of_rank(len, r);
+      if (kt < 0) continue;
+      if (n >= cap) return -2;
+      items[n++] = (uint32_t)((long long)u * ranks + kt);
+    }
+  }
+  off[sc.n_ctas] = n;
   return n;
 }
 
@@ -834,9 +904,8 @@ cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   bp.drop = drop_params_of(p);
   cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16, kDrop, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
-  dim3 grid((p.N + kTile - 1) / kTile, p.H, p.B);
-  if (build_sched(p, bp.sched)) grid = dim3(bp.sched.n_ctas, 1, 1);
-  tc_bwd128_kernel<F16, kDrop, kDq><<<grid, kThreads, kSmemBytes, s>>>(bp);
+  if (!build_sched(p, bp.sched)) return note_error("backward schedule (no multiprocessor count, or more than 2^31 work items)", cudaErrorInvalidValue);
+  tc_bwd128_kernel<F16, kDrop, kDq><<<bp.sched.n_ctas, kThreads, kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }

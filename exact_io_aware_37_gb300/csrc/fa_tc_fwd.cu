@@ -4,9 +4,8 @@
 // "FlashAttention" section 6 with the running softmax of section 5: a CTA
 // works on two 128-row query tiles of one (sequence, head) at a time (a
 // pair), loads them once, and visits the allowed 128-key K/V tiles in turn;
-// for dense inputs it is persistent and works through a host-built list of
-// pairs (see FwdSched).  The score tile and the
-// output accumulator never leave the SM: S = Q K^T and u += P V are tcgen05
+// it is persistent and works through a list of pairs (see FwdSched).  The
+// score tile and the output accumulator never leave the SM: S = Q K^T and u += P V are tcgen05
 // MMAs whose accumulators live in tensor memory (TMEM), and only O = u / l and
 // L = m + log(l) are written to device memory (section 7).
 //
@@ -47,6 +46,7 @@
 
 #include "fa_dropout.cuh"
 #include "fa_internal.cuh"
+#include "fa_sched.cuh"
 #include "fa_tmap.cuh"
 #include "ptx.cuh"
 
@@ -63,18 +63,24 @@ constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 constexpr int kFwdHeadGroup = 16;  // heads per group of the causal block order (measured best of 8..64)
 
-// A persistent launch hands each CTA a list of query-tile pairs worked out on
-// the host (the causal heavy-first order, each pair to the CTA with the least
-// work so far), so the CTA launch, tensor-memory allocation and first loads
-// are paid once per CTA and a pair's epilogue overlaps the next pair's loads.
+// Each CTA of the (always persistent) launch walks a list of query-tile pairs
+// (fa_sched.cuh): the CTA launch, tensor-memory allocation and first loads are
+// paid once per CTA and a pair's epilogue overlaps the next pair's loads.
+// Dense inputs of at most kMaxSchedItems pairs get a host-built table (the
+// causal heavy-first order inside groups of heads, each pair to the CTA with
+// the least work so far); larger and packed inputs the closed-form list.
 constexpr int kMaxSchedCtas = 160;
 constexpr int kMaxSchedItems = 4096;
+constexpr int kSchedTable = 0, kSchedClosed = 1;
 
 struct FwdSched {
-  int n_ctas;                       // 0: one pair per CTA, taken from the grid
-  int n_pairs;                      // pairs per (b, h)
-  uint16_t off[kMaxSchedCtas + 1];  // CTA c works on item[off[c] .. off[c + 1])
-  uint32_t item[kMaxSchedItems];    // (b * H + h) * n_pairs + pair
+  int n_ctas;                       // CTAs of the launch
+  int mode;                         // kSchedTable or kSchedClosed
+  int n_pairs;                      // table: pairs per (b, h)
+  uint32_t n_virtual;               // closed form: (B * H) * ranks
+  uint32_t per, ranks, snake;       // closed form: units per group, pairs per unit, CTA order
+  uint16_t off[kMaxSchedCtas + 1];  // table: CTA c works on item[off[c] .. off[c + 1])
+  uint32_t item[kMaxSchedItems];    // table: (b * H + h) * n_pairs + pair
 };
 
 struct FwdParams {
@@ -130,34 +136,53 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     int b, h, len, row0, slab, qt0, nkv0, nkv1, nmax, t_last;
     long long out_base;
   };
-  const bool persistent = p.sched.n_ctas > 0;
-  int n_items = 1, first_item = 0;
-  if (persistent) {
-    first_item = p.sched.off[blockIdx.x];
-    n_items = p.sched.off[blockIdx.x + 1] - first_item;
-  }
-  auto pair_at = [&](int ii) {
-    Pair q;
-    int pair;
-    if (persistent) {  // dense: every listed pair is in range
-      const uint32_t code = p.sched.item[first_item + ii];
+  const bool table = p.sched.mode == kSchedTable;
+  const int first_item = table ? p.sched.off[blockIdx.x] : 0;
+  const int n_table = table ? p.sched.off[blockIdx.x + 1] - first_item : 0;
+  const ClosedSpec closed{p.sched.n_virtual, (uint32_t)p.B * (uint32_t)p.H, p.sched.per, p.sched.ranks,
+                          (uint32_t)p.sched.n_ctas, p.sched.snake};
+  // steps of the two query tiles of pair `pair` of q's sequence
+  auto set_geometry = [&](Pair& q, int pair) {
+    const int n_qt = (q.len + kBM - 1) / kBM;
+    const int n_kv = (q.len + kBN - 1) / kBN;
+    q.qt0 = 2 * pair;
+    q.nkv0 = p.causal ? min(q.qt0 + 1, n_kv) : n_kv;
+    q.nkv1 = q.qt0 + 1 < n_qt ? (p.causal ? min(q.qt0 + 2, n_kv) : n_kv) : 0;
+    q.nmax = max(q.nkv0, q.nkv1);
+    q.t_last = q.nkv1 > 0 ? 1 : 0;  // its MMAs are issued last in every step; its count is nmax
+  };
+  // The CTA's next pair after list position k (k moves past it); false once
+  // the list has ended.  Every role walks the same list.
+  auto next_pair = [&](uint32_t& k, Pair& q) -> bool {
+    if (table) {  // dense: every listed pair is in range
+      if (k >= (uint32_t)n_table) return false;
+      const uint32_t code = p.sched.item[first_item + (int)k++];
       const int bh = (int)(code / (uint32_t)p.sched.n_pairs);
-      pair = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_pairs);
+      const int pair = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_pairs);
       q.b = bh / p.H;
       q.h = bh - q.b * p.H;
       q.len = p.N;
       q.row0 = 0;
       q.slab = bh;
       q.out_base = (long long)bh * p.N;
-    } else {
-      // causal: pairs of late query tiles see the most keys and are handed out first
-      const GridItem g = p.causal ? grouped_heavy_first(kFwdHeadGroup)
-                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
-      q.b = g.b;
-      q.h = g.h;
-      pair = p.causal ? (int)gridDim.x - 1 - g.rank : g.rank;
+      set_geometry(q, pair);
+      return true;
+    }
+    for (;;) {
+      const uint32_t f = closed_item(closed, blockIdx.x, k);
+      if (f >= closed.n_virtual) return false;
+      ++k;
+      uint32_t uu, rr;
+      closed_unit_rank(closed, f, uu, rr);
+      const int r = (int)rr, u = (int)uu;
+      q.b = u / p.H;
+      q.h = u - q.b * p.H;
       if (p.cu != nullptr) {
         const int s0 = p.cu[q.b], s1 = p.cu[q.b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {  // skipped and reported
+          if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
+          continue;
+        }
         q.len = s1 - s0;
         q.row0 = s0;
         q.slab = q.h;
@@ -165,33 +190,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       } else {
         q.len = p.N;
         q.row0 = 0;
-        q.slab = q.b * p.H + q.h;
-        q.out_base = (long long)q.slab * p.N;
+        q.slab = u;
+        q.out_base = (long long)u * p.N;
       }
+      const int pair = fwd_pair_of_rank(q.len, r, p.causal);
+      if (pair < 0) continue;  // the sequence has fewer pairs
+      set_geometry(q, pair);
+      return true;
     }
-    const int n_qt = (q.len + kBM - 1) / kBM;
-    const int n_kv = (q.len + kBN - 1) / kBN;
-    q.qt0 = 2 * pair;
-    const bool in = pair < (n_qt + 1) / 2;
-    q.nkv0 = !in ? 0 : p.causal ? min(q.qt0 + 1, n_kv) : n_kv;
-    q.nkv1 = (in && q.qt0 + 1 < n_qt) ? (p.causal ? min(q.qt0 + 2, n_kv) : n_kv) : 0;
-    q.nmax = max(q.nkv0, q.nkv1);
-    q.t_last = q.nkv1 > 0 ? 1 : 0;  // its MMAs are issued last in every step; its count is nmax
-    return q;
   };
-  if (!persistent) {
-    if (p.cu != nullptr) {
-      const GridItem g = p.causal ? grouped_heavy_first(kFwdHeadGroup)
-                                  : GridItem{(int)blockIdx.x, (int)blockIdx.z, (int)blockIdx.y};
-      const int s0 = p.cu[g.b], s1 = p.cu[g.b + 1];
-      if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {
-        if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
-        return;
-      }
-    }
-    if (pair_at(0).nmax <= 0) return;
+  {
+    uint32_t k0 = 0;
+    Pair first;
+    if (!next_pair(k0, first)) return;  // nothing for this CTA
   }
-  if (n_items <= 0) return;
 
   if (threadIdx.x == 0) {
     mbar_init(&bar_q, 1);
@@ -232,8 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     bool ok = true;
     int G = 0;   // steps of the earlier pairs
     int cs = 0;  // completions of bar_s[t] seen so far
-    for (int ii = 0; ok && ii < n_items; ++ii) {
-      const Pair q = pair_at(ii);
+    uint32_t cur = 0;
+    Pair q;
+    while (ok && next_pair(cur, q)) {
       const int n = t == 0 ? q.nkv0 : q.nkv1;
       const int len = q.len;
       if (n > 0) {
@@ -401,13 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       // the barrier it polls needs a load issued after the wait.
       int issued = 0, q_issued = 0, G = 0;
       bool good = true;
-      Pair q = pair_at(0);
+      uint32_t cur = 0;
+      Pair q, nx;
+      next_pair(cur, q);  // the CTA has at least one pair
       load_q(q, 1);
       load_k(q, 0, 0, &bar_q);
       q_issued = 1;
-      for (int ii = 0; good && ii < n_items; ++ii) {
-        const bool has_next = ii + 1 < n_items;
-        const Pair nx = has_next ? pair_at(ii + 1) : q;
+      bool have = true;
+      for (int ii = 0; good && have; ++ii) {
+        const bool has_next = next_pair(cur, nx);
         for (int j = 0; j < q.nmax; ++j) {
           const int g = G + j;
           const int s = g % C::kStages;
@@ -443,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           q_issued = ii + 2;
         }
         q = nx;
+        have = has_next;
       }
       if (abort_flag) {
         // let copies already in flight land before the CTA's memory is released
@@ -498,15 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       int G = 0;
       int cp[2] = {0, 0};    // completions of bar_p[t] waited for
       int used[2] = {0, 0};  // pairs that used query tile t so far
-      for (int ii = 0; ok && ii < n_items; ++ii) {
-        // the pair's step counts, without the rest of its geometry (this thread
-        // has few registers to spare)
-        int nk[2];
-        {
-          const Pair q = pair_at(ii);
-          nk[0] = q.nkv0;
-          nk[1] = q.nkv1;
-        }
+      uint32_t cur = 0;
+      Pair q;
+      for (int ii = 0; ok && next_pair(cur, q); ++ii) {
+        // the pair's step counts (the rest of its geometry is not needed here)
+        const int nk[2] = {q.nkv0, q.nkv1};
         const int nmax = max(nk[0], nk[1]);
         // Q tiles (and, for the first pair, K_0; later pairs' K_0 came with the
         // previous pair's last V, whose barrier was waited for); each tile's S goes
@@ -564,16 +576,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 // steps (waiting for its Q tiles, the epilogue); it only steers the balance.
 constexpr int kPairOverheadSteps = 1;
 
-// The work list for at most `ctas_max` CTAs: false (one CTA per pair) for
-// packed inputs, whose sequence lengths live on the device, or when the pairs
-// do not fit the parameter block.
+// The work list for at most `ctas_max` CTAs: the table for dense inputs with
+// at most kMaxSchedItems pairs, the closed-form list otherwise; false when
+// there is nothing to do.
 bool fill_fwd_sched(const Problem& p, int ctas_max, FwdSched& sc) {
   sc.n_ctas = 0;
   const int n_qt = (p.N + kBM - 1) / kBM, n_kv = (p.N + kBN - 1) / kBN;
   const int n_pairs = (n_qt + 1) / 2;
   const long long n_bh = (long long)p.B * p.H;
   const long long n = n_bh * n_pairs;
-  if (p.cu != nullptr || n <= 0 || n > kMaxSchedItems || ctas_max <= 0) return false;
+  if (n <= 0 || ctas_max <= 0) return false;
+  sc.n_pairs = n_pairs;
+  if (p.cu != nullptr || n > kMaxSchedItems) {
+    sc.mode = kSchedClosed;
+    const long long v = n_bh * fwd_ranks(p.N);
+    if (v > (long long)kMaxVirtualItems) return false;
+    sc.n_virtual = (uint32_t)v;
+    sc.per = (uint32_t)n_bh;  // one group: every unit's heaviest pairs first
+    sc.ranks = (uint32_t)fwd_ranks(p.N);
+    sc.snake = 1;
+    sc.n_ctas = (int)std::min<long long>(v, ctas_max);
+    return true;
+  }
+  sc.mode = kSchedTable;
+  sc.n_virtual = (uint32_t)n;
   const int ctas = (int)std::min<long long>(n, std::min(ctas_max, kMaxSchedCtas));
   // Pairs in the order the grid used: with the mask, heaviest first inside
   // balanced groups of kFwdHeadGroup heads (the order of grouped_heavy_first).
@@ -615,7 +641,6 @@ bool fill_fwd_sched(const Problem& p, int ctas_max, FwdSched& sc) {
   }
   sc.off[ctas] = (uint16_t)at;
   sc.n_ctas = ctas;
-  sc.n_pairs = n_pairs;
   return true;
 }
 
@@ -627,8 +652,9 @@ bool build_fwd_sched(const Problem& p, FwdSched& sc) {
   static long long key[5] = {-1, -1, -1, -1, -1};
   static FwdSched cached;
   const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  if (p.cu != nullptr) return fill_fwd_sched(p, ctas, sc);  // closed form: nothing to cache
   std::lock_guard<std::mutex> lock(mu);
-  if (p.cu == nullptr && std::equal(want, want + 5, key)) {
+  if (std::equal(want, want + 5, key)) {
     sc = cached;
     return true;
   }
@@ -661,25 +687,54 @@ cudaError_t launch_fwd_d(const Problem& p, cudaStream_t s) {
   fp.drop = drop_params_of(p);
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, F16, kDrop>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("forward smem attribute", e);
-  const int n_qt = (p.N + kBM - 1) / kBM;
-  dim3 grid((n_qt + 1) / 2, p.H, p.B);
-  if (build_fwd_sched(p, fp.sched)) grid = dim3(fp.sched.n_ctas, 1, 1);
-  tc_fwd_kernel<D, F16, kDrop><<<grid, kThreads, C::kSmemBytes, s>>>(fp);
+  if (!build_fwd_sched(p, fp.sched)) return note_error("forward schedule (no multiprocessor count, or more than 2^31 work items)", cudaErrorInvalidValue);
+  tc_fwd_kernel<D, F16, kDrop><<<fp.sched.n_ctas, kThreads, C::kSmemBytes, s>>>(fp);
   note_launches(1);
   return note_error("forward launch", cudaGetLastError());
 }
 
 }  // namespace
 
-int preview_fwd_schedule(const Problem& p, int ctas, uint16_t* off, uint32_t* items, int cap) {
+int preview_fwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int* off, uint32_t* items, int cap,
+                         int* form) {
   static FwdSched sc;  // large; previews are a host-side test aid
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (!fill_fwd_sched(p, ctas, sc)) return -1;
-  const int n = sc.off[sc.n_ctas];
-  if (n > cap) return -2;
-  std::copy(sc.off, sc.off + sc.n_ctas + 1, off);
-  std::copy(sc.item, sc.item + n, items);
+  *form = sc.mode;
+  if (sc.mode == kSchedTable) {
+    const int n = sc.off[sc.n_ctas];
+    if (n > cap) return -2;
+    for (int c = 0; c <= sc.n_ctas; ++c) off[c] = sc.off[c];
+    std::copy(sc.item, sc.item + n, items);
+    return n;
+  }
+  // the closed form, walked exactly as the kernel's roles walk it
+  const ClosedSpec closed{sc.n_virtual, (uint32_t)p.B * (uint32_t)p.H, sc.per, sc.ranks, (uint32_t)sc.n_ctas,
+                          sc.snake};
+  const int ranks = fwd_ranks(p.N);
+  int n = 0;
+  for (int c = 0; c < sc.n_ctas; ++c) {
+    off[c] = n;
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t f = closed_item(closed, (uint32_t)c, k);
+      if (f >= closed.n_virtual) break;
+      uint32_t uu, rr;
+      closed_unit_rank(closed, f, uu, rr);
+      const int r = (int)rr, u = (int)uu;
+      int len = p.N;
+      if (cu_host != nullptr) {
+        const int b = u / p.H, s0 = cu_host[b], s1 = cu_host[b + 1];
+        if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) continue;
+        len = s1 - s0;
+      }
+      const int pair = fwd_pair_of_rank(len, r, p.causal);
+      if (pair < 0) continue;
+      if (n >= cap) return -2;
+      items[n++] = (uint32_t)((long long)u * ranks + pair);
+    }
+  }
+  off[sc.n_ctas] = n;
   return n;
 }
 

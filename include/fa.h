@@ -224,27 +224,48 @@ const char* fa_last_error_detail(void);
 void fa_bwd_time_main_kernel(void* start_event, void* stop_event);
 
 /*
+ * Instrumentation: measured throughput of the GPU's special-function units
+ * for ex2.approx.f32, the instruction the kernels use for every attention
+ * weight (tensortonic.com "FlashAttention", section 5: each weight is an
+ * exponential of a shifted score).  Launches one CTA per SM in which every
+ * thread runs 8 independent 2^(-x) recurrences for `iters` rounds (1 ..
+ * 2^20) between two reads of the SM clock, waits for it, and writes the mean
+ * over CTAs of exponentials per clock per SM to *ex2_per_clk_per_sm (host
+ * pointer).  Synchronises `stream`.  FA_ERR_INVALID for a NULL pointer or
+ * iters out of range, FA_ERR_CUDA if a CUDA call fails.
+ */
+fa_status fa_probe_ex2_rate(int iters, double* ex2_per_clk_per_sm, void* stream);
+
+/*
  * Number of kernels this library has launched in this process (all devices,
  * all entry points, including failed launches it detected).  Host only.
  */
 unsigned long long fa_launch_count(void);
 
 /*
- * Host-only view of the work list a persistent launch uses for dense inputs
- * of B x H x N (instrumentation and tests; no GPU needed).  kernel 0 = the
- * tensor-core forward, whose items are pairs of 128-row query tiles,
- * code = (b * H + h) * n_pairs + pair; kernel 1 = the D = 128 backward,
- * whose items are 128-key tiles, code = (b * H + h) * n_kt + kt.  The items
- * are taken in the order the one-CTA-per-item grid would hand them out and
- * each goes to the CTA with the least work so far; at most min(n_ctas, 160)
- * CTAs get work.  Writes off[0 .. c] (off must hold n_ctas + 1 entries;
- * CTA i works on items[off[i] .. off[i + 1]), in that order) and returns the
- * number of items; -1 for arguments out of range or problems too large for a
- * persistent launch (more than 4096 items), -2 if `cap` is below the item
- * count.
+ * Host-only view of the work lists of the persistent tensor-core launches
+ * (instrumentation and tests; no GPU needed).  kernel 0 = the forward, whose
+ * items are pairs of 128-row query tiles; kernel 1 = the D = 128 backward,
+ * whose items are 128-key tiles.  cu_seqlens: NULL for dense input, else a
+ * HOST copy of the packed offsets (int32[B+1]).  Two forms (written to
+ * *form): 0 = a table worked out on the host, for dense inputs of at most
+ * 4096 items -- items in the order the one-CTA-per-item grid would hand them
+ * out (heaviest first inside groups of heads), each to the CTA with the least
+ * work so far, at most min(n_ctas, 160) CTAs; 1 = the closed-form list, for
+ * larger or packed inputs -- units u = b * H + h cut into groups (the
+ * backward: about 4 units each; the forward: one group), inside a group the
+ * units' items rank-major, heaviest first, virtual item f counting the groups
+ * one after the other; CTA c of n = min(n_ctas, B * H * ranks) takes
+ * f = k * n + c (backward), or k * n + c for even k and k * n + n - 1 - c
+ * for odd k (forward), skipping the ranks its sequence does not have.
+ * Item codes are u * R + pair (forward) or u * R + key tile (backward), with
+ * R = ceil(ceil(N / 128) / 2) pairs or ceil(N / 128) key tiles.  Writes
+ * off[0 .. c] (off must hold n_ctas + 1 entries; CTA i works on
+ * items[off[i] .. off[i + 1]), in that order) and returns the number of
+ * items; -1 for arguments out of range, -2 if `cap` is below the item count.
  */
-int fa_schedule_preview(int kernel, int B, int H, int N, int causal, int n_ctas, unsigned short* off,
-                        unsigned int* items, int cap);
+int fa_schedule_preview(int kernel, const int32_t* cu_seqlens, int B, int H, int N, int causal, int n_ctas,
+                        int* off, unsigned int* items, int cap, int* form);
 
 /* Attention dropout (tensortonic.com "FlashAttention" section 7: the backward
  * must reproduce the forward's dropout decisions from saved generator state).

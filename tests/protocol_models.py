@@ -188,7 +188,10 @@ def run_forward(pairs, seed, S=2, skip=()):
 
 
 def run_backward(items, seed, skip=()):
-    """items: list of step counts (one per key tile of this CTA)."""
+    """items: list of step counts (one per key tile of this CTA).  The MMA
+    thread knows only how many tiles there are; each tile's step count reaches
+    it through a two-slot shared-memory ring the producer fills before arming
+    the tile's K / V barrier."""
     rng = random.Random(seed)
     B = lambda n, c=1: Bar(n, c)
     kv = B("kv"); qf = [B("qf0", 2), B("qf1", 2)]; qe = [B("qe0"), B("qe1")]; of = B("of"); oe = B("oe")
@@ -204,6 +207,7 @@ def run_backward(items, seed, skip=()):
     tm = {"DP": None, "S": None, "acc": None}   # tensor-memory contents (what the last writer put there)
     drained = set()    # dQ steps read out of TMEM
     acc_read = set()   # items whose dK/dV the epilogue read out
+    steps_ring = [None, None]  # (tile, step count) per slot
     def rd(k, d): reads[k] = reads.get(k, 0) + d
     def issue(op):
         pipe.append(op)
@@ -238,6 +242,7 @@ def run_backward(items, seed, skip=()):
     def producer():
         G = 0
         def load_kv(ii):
+            steps_ring[ii & 1] = (ii, items[ii])
             kv.arrive(tx=2); loads.append(("K", ii, kv, 1)); loads.append(("V", ii, kv, 1))
         for ii, n in enumerate(items):
             if ii == 0: load_kv(0)
@@ -259,8 +264,10 @@ def run_backward(items, seed, skip=()):
             G += n
     def mma():
         G = 0
-        for ii, n in enumerate(items):
+        for ii in range(len(items)):
             while not kv.try_wait(ii & 1): yield
+            tag, n = steps_ring[ii & 1]
+            assert tag == ii, f"MMA thread reads the step count of tile {tag} for tile {ii}"
             while not qf[G & 1].try_wait((G >> 1) & 1): yield
             issue(("S", {"g": G, "want": [ii, G]}, ["K", f"Q{G & 1}"])); issue(("commit", {"bar": bs, "want": []}, []))
             if G > 0:

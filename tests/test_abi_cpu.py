@@ -6,6 +6,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 import pytest
 import torch
 
@@ -210,50 +212,107 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 # Work lists of the persistent launches (host logic, no GPU).  Weights are the
-# per-item step counts plus the per-item overheads the schedulers charge:
+# per-item step counts plus the per-item overheads the table builder charges:
 # 1 step for a forward query-tile pair, 2 for a backward key tile.
-def _preview(lib, kernel, B, H, N, causal, ctas):
-    off = (ctypes.c_ushort * (ctas + 1))()
-    cap = 4096
+def _preview(lib, kernel, B, H, N, causal, ctas, lengths=None, cap=1 << 17):
+    cu = None
+    if lengths is not None:
+        cu = (ctypes.c_int32 * (len(lengths) + 1))(*([0] + list(np.cumsum(lengths))))
+    off = (ctypes.c_int * (ctas + 1))()
     items = (ctypes.c_uint * cap)()
-    n = lib.fa_schedule_preview(kernel, B, H, N, causal, ctas, off, items, cap)
-    return n, list(off), list(items[:max(n, 0)])
+    form = ctypes.c_int(-1)
+    n = lib.fa_schedule_preview(kernel, cu, B, H, N, causal, ctas, off, items, cap, ctypes.byref(form))
+    return n, list(off), list(items[:max(n, 0)]), form.value
 
 
-def _weights(kernel, H, B, N, causal):
-    n_t = (N + 127) // 128
-    if kernel == 0:
-        n_pairs = (n_t + 1) // 2
-        per = [(min(2 * pr + 2, n_t) if causal else n_t) + 1 for pr in range(n_pairs)]
-    else:
-        per = [(n_t - kt if causal else n_t) + 2 for kt in range(n_t)]
-    return {bh * len(per) + u: w for bh in range(B * H) for u, w in enumerate(per)}
+def _weights(kernel, H, B, N, causal, lengths=None):
+    """code -> weight of every real item (codes as fa_schedule_preview writes them)."""
+    lens = lengths if lengths is not None else [N] * B
+    ranks = ((N + 127) // 128 + 1) // 2 if kernel == 0 else (N + 127) // 128
+    out = {}
+    for b, n in enumerate(lens):
+        n_t = (n + 127) // 128
+        for h in range(H):
+            u = b * H + h
+            if kernel == 0:
+                for pr in range((n_t + 1) // 2):
+                    out[u * ranks + pr] = (min(2 * pr + 2, n_t) if causal else n_t) + 1
+            else:
+                for kt in range(n_t):
+                    out[u * ranks + kt] = (n_t - kt if causal else n_t) + 2
+    return out
+
+
+def _loads(n, off, items, weight, used):
+    assert n == len(weight)
+    assert sorted(items) == sorted(weight)          # every item exactly once
+    assert off[0] == 0 and off[used] == n
+    assert all(off[c] <= off[c + 1] for c in range(used))
+    return [sum(weight[code] for code in items[off[c]:off[c + 1]]) for c in range(used)]
 
 
 @pytest.mark.parametrize("kernel,B,H,N,causal,ctas", [
     (0, 2, 32, 4096, 1, 152), (0, 2, 32, 4096, 0, 152), (1, 2, 32, 4096, 1, 152), (1, 2, 32, 4096, 0, 152),
     (0, 4, 16, 1024, 1, 152), (1, 4, 16, 1024, 1, 152), (0, 1, 3, 300, 1, 152), (1, 1, 3, 300, 0, 7),
     (0, 1, 32, 32768, 1, 152), (1, 2, 5, 2000, 1, 64)])
-def test_persistent_schedule_covers_and_balances(lib, kernel, B, H, N, causal, ctas):
-    n, off, items = _preview(lib, kernel, B, H, N, causal, ctas)
+def test_persistent_table_covers_and_balances(lib, kernel, B, H, N, causal, ctas):
+    n, off, items, form = _preview(lib, kernel, B, H, N, causal, ctas)
+    assert form == 0                                  # dense, at most 4096 items: the host table
     weight = _weights(kernel, H, B, N, causal)
-    assert n == len(weight)
-    # every item exactly once
-    assert sorted(items) == sorted(weight)
-    used = min(ctas, 160, n)
-    assert off[0] == 0 and off[used] == n
-    assert all(off[c] <= off[c + 1] for c in range(used))
-    loads = [sum(weight[code] for code in items[off[c]:off[c + 1]]) for c in range(used)]
+    loads = _loads(n, off, items, weight, min(ctas, 160, n))
     # greedy assignment to the least-loaded CTA: no CTA ends more than one item heavier than another
     assert max(loads) - min(loads) <= max(weight.values())
-    # and no CTA gets more than one item above the average
-    assert max(loads) <= sum(loads) / used + max(weight.values())
+    assert max(loads) <= sum(loads) / len(loads) + max(weight.values())
+
+
+@pytest.mark.parametrize("kernel,B,H,N,causal", [
+    (1, 1, 32, 32768, 1),     # 8192 key tiles: the long-window backward
+    (0, 1, 64, 32768, 1),     # 8192 pairs
+    (1, 4, 32, 8192, 0),      # 8192 key tiles, no mask
+    (0, 3, 40, 12345, 1)])    # ragged length
+def test_persistent_closed_form_dense(lib, kernel, B, H, N, causal):
+    """Beyond 4096 items the closed form: every item once, heaviest ranks first
+    across all heads, a snake over the CTAs; for a list sorted by weight the
+    snake keeps every CTA within one item of the average."""
+    ctas = 152
+    n, off, items, form = _preview(lib, kernel, B, H, N, causal, ctas)
+    assert form == 1
+    weight = _weights(kernel, H, B, N, causal)
+    loads = _loads(n, off, items, weight, ctas)
+    avg = sum(loads) / ctas
+    assert max(loads) <= avg + max(weight.values())
+    assert min(loads) >= avg - max(weight.values())
+    # CTA 0 takes virtual items 0, 2P-1, 2P, 4P-1, ...: its first item is unit 0's heaviest
+    ranks = ((N + 127) // 128 + 1) // 2 if kernel == 0 else (N + 127) // 128
+    first = items[off[0]]
+    assert first // ranks == 0 and weight[first] == max(weight.values())
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_persistent_closed_form_packed(lib, kernel, causal):
+    """Packed sequences (the 16-sequence workload's seeded lengths): every
+    (sequence, head) item once, none of a sequence of length 0 or of a
+    malformed sequence, and every CTA within 10 % of the ideal finish time."""
+    from exact_io_aware_37_gb300 import synth
+    lengths = synth.varlen_lengths(16, 128, 8192).tolist()
+    H, N = 32, max(lengths)
+    n, off, items, form = _preview(lib, kernel, len(lengths), H, N, causal, 152, lengths=lengths)
+    assert form == 1
+    weight = _weights(kernel, H, len(lengths), N, causal, lengths)
+    loads = _loads(n, off, items, weight, 152)
+    ideal = max(sum(loads) / 152, max(weight.values()))
+    assert max(loads) <= 1.1 * ideal
+    # empty sequences contribute nothing; small problems use fewer CTAs than SMs
+    lens2 = [300, 0, 129, 1]
+    n2, off2, items2, _ = _preview(lib, kernel, 4, 2, 300, causal, 152, lengths=lens2)
+    weight2 = _weights(kernel, 2, 4, 300, causal, lens2)
+    used = 4 * 2 * (((300 + 127) // 128 + 1) // 2 if kernel == 0 else (300 + 127) // 128)
+    _loads(n2, off2, items2, weight2, used)
 
 
 def test_persistent_schedule_refusals(lib):
-    assert _preview(lib, 0, 1, 64, 65536, 1, 152)[0] == -1      # 64 heads x 256 pairs > 4096 items
     assert _preview(lib, 2, 1, 1, 128, 1, 152)[0] == -1         # no such kernel
     assert _preview(lib, 0, 1, 1, 0, 1, 152)[0] == -1           # empty problem
-    off = (ctypes.c_ushort * 153)()
-    items = (ctypes.c_uint * 4)()
-    assert lib.fa_schedule_preview(1, 2, 32, 4096, 1, 152, off, items, 4) == -2
+    assert _preview(lib, 1, 2, 32, 4096, 1, 152, cap=4)[0] == -2
+    assert _preview(lib, 1, 1, 32, 32768, 1, 152, cap=100)[0] == -2
