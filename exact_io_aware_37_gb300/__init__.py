@@ -206,7 +206,7 @@ def fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, 
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if workspace is None:
         rows = (H * T) if cu_seqlens is not None else (B * H * N)
-        workspace = torch.empty(max((rows * 4 + 255) // 256 * 256, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty((rows * 4 + 255) // 256 * 256 + 256, dtype=torch.uint8, device=q.device)
     st = lib().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                     _ptr(dv), B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T,
                                     _DT[q.dtype], float(p_drop), int(seed), int(offset), _ptr(workspace),

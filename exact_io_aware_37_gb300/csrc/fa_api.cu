@@ -101,6 +101,10 @@ fa_status check_tensor(const void* p) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The tensor-core backward's tile counter (see fa_tc_bwd128.cu), at the end of
+// the workspace; one 256-byte block keeps the workspace's parts aligned.
+constexpr size_t kQueueBytes = 256;
+
 // Attention dropout arguments (nullptr: none).
 struct DropArgs {
   float p;
@@ -259,7 +263,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int D, const int32_t* cu, int 
   if (B < 0 || H < 0 || N < 0 || D <= 0 || (cu && T < 0)) return 0;
   const long long rows = row_count(B, H, N, cu, T);
   size_t bytes = round_up((size_t)rows * sizeof(float), 256);
-  if (use_tensor_cores(dt, D)) bytes += round_up((size_t)rows * D * sizeof(float), 256);
+  if (use_tensor_cores(dt, D)) bytes += round_up((size_t)rows * D * sizeof(float), 256) + kQueueBytes;
   return bytes;
 }
 
@@ -302,7 +306,8 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
   if (!aligned(lse, 4)) return FA_ERR_ALIGN;
   if (cu != nullptr && !aligned(cu, 4)) return FA_ERR_ALIGN;
   // the deterministic path keeps no float32 dQ accumulator: only D_i
-  const size_t need = deterministic ? round_up((size_t)row_count(B, H, N, cu, T) * sizeof(float), 256)
+  const size_t need = deterministic ? round_up((size_t)row_count(B, H, N, cu, T) * sizeof(float), 256) +
+                                          (use_tensor_cores(dt, D) ? kQueueBytes : 0)
                                     : fa_bwd_workspace_size(B, H, N, D, cu, T, dt);
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
 
@@ -319,6 +324,9 @@ static fa_status bwd_impl(const void* q, const void* k, const void* v, const voi
   p.dq_acc = use_tensor_cores(dt, D) && !deterministic
                  ? reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)rows * 4, 256))
                  : nullptr;
+  // the tensor-core backward's tile counter: the last kQueueBytes of the workspace it needs
+  p.queue = use_tensor_cores(dt, D) ? reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + need - kQueueBytes)
+                                    : nullptr;
   g_detail[0] = 0;
   cudaEvent_t ev_start = g_main_start, ev_stop = g_main_stop;
   g_main_start = g_main_stop = nullptr;

@@ -37,6 +37,7 @@ struct Problem {
   void* dv;
   float* dvec;      // D_i workspace (backward)
   float* dq_acc;    // float32 dQ accumulator (backward, tensor-core path)
+  unsigned* queue;  // tile counter of the backward's queue (workspace; zeroed by the preprocess kernel)
   int B, H, N, D;
   int T;            // packed token count (0 when dense)
   int f16;          // 16-bit tensors: 1 = fp16, 0 = bf16
@@ -128,7 +129,8 @@ class SymbolAddress {
 
 // Work lists of the persistent forward / backward launches for `ctas` CTAs
 // (host only; see fa_schedule_preview).  cu_host: packed sequence offsets on
-// the host, or nullptr for dense input.  *form: 0 = table, 1 = closed form.
+// the host, or nullptr for dense input.  *form: 0 = table, 1 = closed form
+// (forward), 2 = queue (backward).
 int preview_fwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int* off, uint32_t* items, int cap,
                          int* form);
 int preview_bwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int* off, uint32_t* items, int cap,

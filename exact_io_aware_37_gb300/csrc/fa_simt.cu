@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(Problem p, long lon
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) p.dvec[warp] = acc;
+  if (warp == 0 && lane == 0 && p.queue != nullptr) *p.queue = 0u;  // the backward's tile counter
   if (zero_acc) {
     float4* row = reinterpret_cast<float4*>(p.dq_acc + warp * p.D);
     for (int c = lane; c < p.D / 4; c += 32) row[c] = make_float4(0.f, 0.f, 0.f, 0.f);

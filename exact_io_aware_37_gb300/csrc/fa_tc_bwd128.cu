@@ -6,9 +6,9 @@
 // saved log-sum-exp; dV = P^T dO, dS = P o (dO V^T - D), dK = scale dS^T Q,
 // dQ = scale dS K): a CTA holds one 128-key tile of K and V in shared memory
 // at a time and visits the 128-query tiles that can see it; every launch is
-// persistent and each CTA works through a list of key tiles (fa_sched.cuh:
-// a host-built table for dense inputs that fit one, a closed-form list
-// otherwise).  All five products are
+// persistent: one CTA per SM takes key tiles one after another (see BwdSched)
+// and hands each to its roles through a ring in shared memory.  All five
+// products are
 // tcgen05 MMAs with M = N = 128, placed in tensor memory as
 //     [0,128)   S^T = K Q^T, then P^T (bf16) over its columns [0,32) and [64,96)
 //     [128,256) dP^T = V dO^T, then dS^T (bf16) over [128,160) and [192,224),
@@ -70,26 +70,46 @@ constexpr int kBwdSupportRegs = 136;
 static_assert(2 * 128 * kBwdComputeRegs + 128 * kBwdSupportRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch budget");
 
-// Each CTA of the (always persistent) launch works through a list of key
-// tiles (b, h, kt), so a CTA launch, tensor-memory allocation and pipeline
-// fill are paid once and the next tile's loads and first products overlap
-// the previous tile's last reductions and its dK / dV stores.  Dense inputs
-// of at most kMaxSchedItems tiles get a table worked out on the host: items
-// in the causal heavy-first order inside groups of heads, each given to the
-// CTA with the least work so far (longest processing time first); larger and
-// packed inputs the closed-form list of fa_sched.cuh.
+// Each CTA of the (always persistent) launch works through key tiles
+// (b, h, kt) one after another, so a CTA launch, tensor-memory allocation and
+// pipeline fill are paid once and the next tile's loads and first products
+// overlap the previous tile's last reductions and its dK / dV stores.  The
+// producer warp takes the tiles and hands each to the other roles through a
+// ring of kItemRing records in shared memory (bar_item / bar_itemfree), then
+// an end record.  Where it takes them from:
+//   table    dense inputs of at most kMaxSchedItems tiles: a list per CTA
+//            worked out on the host -- items in the causal heavy-first order
+//            inside groups of heads, each to the CTA with the least work so
+//            far (longest processing time first);
+//   queue    larger and packed inputs: a counter in the caller's workspace
+//            (zeroed by the preprocess kernel) over the same order, written
+//            in closed form over virtual items (fa_sched.cuh: groups of about
+//            kBwdHeadGroup (sequence, head) units, rank-major inside a group,
+//            ranks a sequence does not have skipped by the producer).  CTAs
+//            take the next tile when they need one, as the block scheduler
+//            would, so the tiles in flight stay a contiguous stretch of the
+//            order (their operands stay in L2) and no CTA runs out of work
+//            early.
 constexpr int kMaxSchedCtas = 160;
 constexpr int kMaxSchedItems = 4096;
-constexpr int kSchedTable = 0, kSchedClosed = 1;
+constexpr int kSchedTable = 0, kSchedQueue = 2;
+constexpr int kItemRing = 4;
 
 struct BwdSched {
   int n_ctas;                         // CTAs of the launch
-  int mode;                           // kSchedTable or kSchedClosed
+  int mode;                           // kSchedTable or kSchedQueue
   int n_kt;                           // table: key tiles per (b, h)
-  uint32_t n_virtual;                 // closed form: (B * H) * ranks
-  uint32_t per, ranks, snake;         // closed form: units per group, key tiles per unit, CTA order
+  uint32_t n_virtual;                 // queue: (B * H) * ranks
+  uint32_t per, ranks;                // queue: units per group, key tiles per unit
   uint16_t off[kMaxSchedCtas + 1];    // table: CTA c works on item[off[c] .. off[c + 1])
   uint32_t item[kMaxSchedItems];      // table: (b * H + h) * n_kt + kt
+};
+
+// One key tile as the roles see it: its (b, h) rows and the query tiles that
+// see it.  n_steps < 0 marks the end of the CTA's tiles.
+struct ItemRec {
+  int b, h, kt, len, row0, slab, q_first, n_steps;
+  long long out_base;
 };
 
 struct Bwd128Params {
@@ -102,6 +122,7 @@ struct Bwd128Params {
   __nv_bfloat16* dv;
   const int32_t* cu;
   unsigned* status;
+  unsigned* queue;  // the tile counter of the queue form (workspace, zero at launch)
   unsigned long long limit_ns;
   int B, H, N, T;
   float c2;  // scale * log2(e)
@@ -122,8 +143,9 @@ constexpr int kStageOff = 6 * kTileBytes;   // dQ staging for queries 64-127: [6
 constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
 constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
 constexpr int kBarOff = kDvOff + 1024;
-constexpr int kNumBars = 20;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kNumBars = 20 + 2 * kItemRing;
+constexpr int kRingOff = kBarOff + kNumBars * 8;                    // kItemRing ItemRec
+constexpr int kMiscOff = kRingOff + kItemRing * (int)sizeof(ItemRec);
 constexpr int kSmemBytes = kMiscOff + 16;
 static_assert(kSmemBytes <= 232448, "shared-memory budget");
 
@@ -156,84 +178,53 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_stfree = bars + 17; // half 1's staging buffer read by the copy engine (reducer)
   uint64_t* bar_itemdone = bars + 18; // every product of a key tile complete (its dK / dV final, K / V free)
   uint64_t* bar_accfree = bars + 19;  // dK / dV of a key tile read out of TMEM (8 compute warps)
+  uint64_t* bar_item = bars + 20;     // [kItemRing] a tile's record written (producer)
+  uint64_t* bar_itemfree = bars + 20 + kItemRing;  // [kItemRing] record read (every consumer role)
+  ItemRec* ring = reinterpret_cast<ItemRec*>(smem + kRingOff);
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
-  // step count of key tile ii, in slot ii % 2: written by the producer before
-  // the tile's K / V load is armed on bar_kv, read by the MMA issuer after its
-  // wait on bar_kv (the issuer has no registers to walk the list itself)
-  int* steps_sh = reinterpret_cast<int*>(smem + kMiscOff + 8);
   float* s_l = reinterpret_cast<float*>(smem + kLOff);
   float* s_d = reinterpret_cast<float*>(smem + kDvOff);
 
-  // ---- the key tiles this CTA works on
-  // Geometry of one key tile: its (b, h) rows and the query tiles that see it.
-  struct Item {
-    int b, h, kt, len, row0, slab, q_first, n_steps;
-    long long out_base;
-  };
+  // ---- where the producer takes this CTA's key tiles from (see BwdSched)
   const bool table = p.sched.mode == kSchedTable;
   const int first_item = table ? p.sched.off[blockIdx.x] : 0;
   const int n_table = table ? p.sched.off[blockIdx.x + 1] - first_item : 0;
-  const ClosedSpec closed{p.sched.n_virtual, (uint32_t)p.B * (uint32_t)p.H, p.sched.per, p.sched.ranks,
-                          (uint32_t)p.sched.n_ctas, p.sched.snake};
-  auto set_steps = [&](Item& it) {
+  const ClosedSpec order{p.sched.n_virtual, (uint32_t)p.B * (uint32_t)p.H, p.sched.per, p.sched.ranks, 1u, 0u};
+  auto set_steps = [&](ItemRec& it) {
     const int n_t = (it.len + kTile - 1) / kTile;
     it.q_first = p.causal ? it.kt : 0;  // earlier query tiles never see these keys
     it.n_steps = n_t - it.q_first;
   };
-  // The CTA's next key tile after list position k (k moves past it); false
-  // once the list has ended.  Every role walks the same list.
-  auto next_item = [&](uint32_t& k, Item& it) -> bool {
-    if (table) {  // dense: every listed tile is in range
-      if (k >= (uint32_t)n_table) return false;
-      const uint32_t code = p.sched.item[first_item + (int)k++];
-      const int bh = (int)(code / (uint32_t)p.sched.n_kt);
-      it.kt = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_kt);
-      it.b = bh / p.H;
-      it.h = bh - it.b * p.H;
+  // the tile of virtual item f of the queue, or false for a rank its sequence lacks
+  auto tile_of_virtual = [&](uint32_t f, ItemRec& it) -> bool {
+    uint32_t uu, rr;
+    closed_unit_rank(order, f, uu, rr);
+    const int u = (int)uu;
+    it.b = u / p.H;
+    it.h = u - it.b * p.H;
+    if (p.cu != nullptr) {
+      const int s0 = p.cu[it.b], s1 = p.cu[it.b + 1];
+      if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {  // skipped and reported
+        atomicOr(p.status, kDevBadSeqlens);
+        return false;
+      }
+      it.len = s1 - s0;
+      it.row0 = s0;
+      it.slab = it.h;
+      it.out_base = (long long)it.h * p.T + s0;
+    } else {
       it.len = p.N;
       it.row0 = 0;
-      it.slab = bh;
-      it.out_base = (long long)bh * p.N;
-      set_steps(it);
-      return true;
+      it.slab = u;
+      it.out_base = (long long)u * p.N;
     }
-    for (;;) {
-      const uint32_t f = closed_item(closed, blockIdx.x, k);
-      if (f >= closed.n_virtual) return false;
-      ++k;
-      uint32_t uu, rr;
-      closed_unit_rank(closed, f, uu, rr);
-      const int r = (int)rr, u = (int)uu;
-      it.b = u / p.H;
-      it.h = u - it.b * p.H;
-      if (p.cu != nullptr) {
-        const int s0 = p.cu[it.b], s1 = p.cu[it.b + 1];
-        if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) {  // skipped and reported
-          if (threadIdx.x == 0) atomicOr(p.status, kDevBadSeqlens);
-          continue;
-        }
-        it.len = s1 - s0;
-        it.row0 = s0;
-        it.slab = it.h;
-        it.out_base = (long long)it.h * p.T + s0;
-      } else {
-        it.len = p.N;
-        it.row0 = 0;
-        it.slab = u;
-        it.out_base = (long long)u * p.N;
-      }
-      it.kt = bwd_tile_of_rank(it.len, r);
-      if (it.kt < 0) continue;  // the sequence has fewer key tiles
-      set_steps(it);
-      return true;
-    }
+    it.kt = bwd_tile_of_rank(it.len, (int)rr);
+    if (it.kt < 0) return false;
+    set_steps(it);
+    return true;
   };
-  {
-    uint32_t k0 = 0;
-    Item first;
-    if (!next_item(k0, first)) return;  // nothing for this CTA
-  }
+  if (table && n_table <= 0) return;  // (a table gives every CTA of the launch work)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
@@ -241,7 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       const bool by8 = bar == bar_p || bar == bar_ds || bar == bar_dqfree || bar == bar_accfree;
       const bool by4 = bar == bar_staged || bar == bar_staged + 1;
       const bool by2 = bar == bar_qf || bar == bar_qf + 1;  // Q bytes + L / D written
-      mbar_init(bar, by8 ? 8 : by4 ? 4 : by2 ? 2 : 1);
+      // a record is read by the 8 compute warps, the MMA issuer and the reducer
+      const bool readers = bar >= bar_itemfree && bar < bar_itemfree + kItemRing;
+      mbar_init(bar, readers ? (kDq ? 10 : 9) : by8 ? 8 : by4 ? 4 : by2 ? 2 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -300,9 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     };
 
     int G = 0;
-    uint32_t cur = 0;
-    Item it;
-    for (int ii = 0; ok && next_item(cur, it); ++ii) {
+    for (int ii = 0; ok; ++ii) {
+      // the tile's record (every lane waits: each acquires what the producer released)
+      const int slot = ii % kItemRing;
+      if (!warp_wait(bar_item + slot, (ii / kItemRing) & 1, w)) {
+        ok = false;
+        break;
+      }
+      const ItemRec it = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_itemfree + slot);
+      if (it.n_steps < 0) break;  // no tiles left
       const int b = it.b, h = it.h, len = it.len;
       const int key = it.kt * kTile + j;
       for (int k = 0; ok && k < it.n_steps; ++k) {
@@ -459,12 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       bool good_all = true;
       // K, V of a tile, once every product of the previous tile (their last
       // readers) is complete; lane 0 waits, the answer is broadcast
-      auto load_kv = [&](const Item& it, int ii) {
+      auto load_kv = [&](const ItemRec& it, int ii) {
         int good = 1;
         if (lane == 0) {
           if (ii > 0) good = mbar_wait(bar_itemdone, (ii - 1) & 1, w);
           if (good) {
-            steps_sh[ii & 1] = it.n_steps;  // slot ii - 2 was read before tile ii - 1 began
             mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
             for (int hf = 0; hf < 2; ++hf) {
               tma_load_3d(smem + kKOff + hf * kHalfBytes, &p.tk, bar_kv, hf * 64, it.row0 + it.kt * kTile, it.slab);
@@ -476,9 +476,65 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         if (good) kv_issued = ii + 1;
         return good != 0;
       };
-      uint32_t cur = 0;
-      Item it;
-      for (int ii = 0; good_all && next_item(cur, it); ++ii) {
+      // ---- taking tiles (lane 0) and handing them to the roles
+      uint32_t k_tab = 0;
+      uint32_t reserved = 0;  // queue: the next virtual item, taken one tile ahead
+      if (!table && lane == 0) reserved = atomicAdd(p.queue, 1u);
+      auto take = [&](ItemRec& it) -> bool {
+        if (table) {  // dense: every listed tile is in range
+          if (k_tab >= (uint32_t)n_table) return false;
+          const uint32_t code = p.sched.item[first_item + (int)k_tab++];
+          const int bh = (int)(code / (uint32_t)p.sched.n_kt);
+          it.kt = (int)(code - (uint32_t)bh * (uint32_t)p.sched.n_kt);
+          it.b = bh / p.H;
+          it.h = bh - it.b * p.H;
+          it.len = p.N;
+          it.row0 = 0;
+          it.slab = bh;
+          it.out_base = (long long)bh * p.N;
+          set_steps(it);
+          return true;
+        }
+        for (;;) {
+          const uint32_t f = reserved;
+          if (f >= p.sched.n_virtual) return false;
+          reserved = atomicAdd(p.queue, 1u);  // in flight while this tile is worked on
+          if (tile_of_virtual(f, it)) return true;
+        }
+      };
+      // Tile ii (or the end) into ring slot ii % kItemRing, once every role has
+      // read the record kItemRing tiles back; lane 0 writes, every lane reads the
+      // record back.  Returns 1 for a tile, 0 at the end, -1 if a wait failed.
+      auto next_tile = [&](int ii, ItemRec& it) -> int {
+        const int slot = ii % kItemRing;
+        int state = 1;
+        if (lane == 0) {
+          ItemRec t{};
+          const bool have = take(t);
+          if (ii >= kItemRing && !mbar_wait(bar_itemfree + slot, (ii / kItemRing - 1) & 1, w)) {
+            state = -1;
+          } else {
+            if (!have) t.n_steps = -1;
+            ring[slot] = t;
+            mbar_arrive(bar_item + slot);  // releases the record to the roles' waits
+            if (have && ii > 0)
+              // its K and V wait for the previous tile's last products: have them in L2 by then
+              for (int hf = 0; hf < 2; ++hf) {
+                tma_prefetch_l2_3d(&p.tk, hf * 64, t.row0 + t.kt * kTile, t.slab);
+                tma_prefetch_l2_3d(&p.tv, hf * 64, t.row0 + t.kt * kTile, t.slab);
+              }
+            state = have ? 1 : 0;
+          }
+        }
+        state = __shfl_sync(0xffffffffu, state, 0);
+        __syncwarp();
+        if (state > 0) it = ring[slot];
+        return state;
+      };
+      ItemRec it;
+      int state = next_tile(0, it);
+      if (state < 0) good_all = false;
+      for (int ii = 0; good_all && state > 0; ++ii) {
         // The first tile's K and V go first; a later tile's wait until its first
         // Q, L / D and dO are on their way, which need no more than their buffers.
         if (ii == 0 && !load_kv(it, ii)) break;
@@ -533,17 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
             break;
           }
         }
-        // the next tile's K and V wait for this tile's last products; have them
-        // in L2 by then
-        uint32_t peek = cur;
-        Item nx;
-        if (lane == 0 && next_item(peek, nx)) {
-          for (int hf = 0; hf < 2; ++hf) {
-            tma_prefetch_l2_3d(&p.tk, hf * 64, nx.row0 + nx.kt * kTile, nx.slab);
-            tma_prefetch_l2_3d(&p.tv, hf * 64, nx.row0 + nx.kt * kTile, nx.slab);
-          }
-        }
+        if (!good_all) break;
         G += it.n_steps;
+        state = next_tile(ii + 1, it);
+        if (state < 0) good_all = false;
       }
       if (lane == 0 && *abort_flag) {
         // let copies already in flight land before the CTA's memory is released
@@ -558,9 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       // handed back as soon as it has been read, half 1's after that.
       int G = 0;
       bool good = true;
-      uint32_t cur = 0;
-      Item it;
-      while (good && next_item(cur, it)) {
+      for (int ii = 0; good; ++ii) {
+        const int slot = ii % kItemRing;
+        if (!mbar_wait(bar_item + slot, (ii / kItemRing) & 1, w)) break;
+        const ItemRec it = ring[slot];
+        mbar_arrive(bar_itemfree + slot);
+        if (it.n_steps < 0) break;  // no tiles left
         for (int kk = 0; good && kk < it.n_steps; ++kk) {
           const int gg = G + kk;
           const int q0 = (it.q_first + kk) * kTile;
@@ -629,21 +681,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       };
       bool ok = true;
       int G = 0;
-      // the CTA's tile count, walked once before the loop (whose registers
-      // the walk would otherwise crowd); each tile's step count comes from
-      // the producer through steps_sh
-      int n_items = 0;
-      {
-        uint32_t cur = 0;
-        Item it;
-        while (next_item(cur, it)) ++n_items;
-      }
-      for (int ii = 0; ok && ii < n_items; ++ii) {
+      for (int ii = 0; ok; ++ii) {
+        // the tile's step count from its record (the issuer has no registers
+        // to spare for the rest of the tile's geometry)
+        const int slot = ii % kItemRing;
+        if (!mbar_wait(bar_item + slot, (ii / kItemRing) & 1, w)) {
+          ok = false;
+          break;
+        }
+        const int n_steps = ring[slot].n_steps;
+        mbar_arrive(bar_itemfree + slot);
+        if (n_steps < 0) break;  // no tiles left
         // K, V of this tile; S^T and dP^T of its first step.  dP^T goes over the
         // previous tile's last dQ^T, so it waits until that has been read out.
         ok = mbar_wait(bar_kv, ii & 1, w) && mbar_wait(bar_qf + (G & 1), (G >> 1) & 1, w);
         if (!ok) break;
-        const int n_steps = steps_sh[ii & 1];
         tc_fence_after();
         issue_s(G);
         ok = (!kDq || G == 0 || mbar_wait(bar_dqfree, (G - 1) & 1, w)) && mbar_wait(bar_of, G & 1, w);
@@ -749,9 +801,9 @@ int sm_count() {
 // balance of the schedule.
 constexpr int kItemOverheadSteps = 2;
 
-// The work list for at most `ctas_max` CTAs: the table for dense inputs with
-// at most kMaxSchedItems key tiles, the closed-form list otherwise; false when
-// there is nothing to do.
+// The schedule for at most `ctas_max` CTAs: the table for dense inputs with
+// at most kMaxSchedItems key tiles, the queue otherwise; false when there is
+// nothing to do.
 bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
   sc.n_ctas = 0;
   const int n_kt = (p.N + kTile - 1) / kTile;
@@ -760,13 +812,12 @@ bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
   if (n <= 0 || ctas_max <= 0) return false;
   sc.n_kt = n_kt;
   if (p.cu != nullptr || n > kMaxSchedItems) {
-    sc.mode = kSchedClosed;
+    sc.mode = kSchedQueue;
     const long long v = n_bh * bwd_ranks(p.N);
     if (v > (long long)kMaxVirtualItems) return false;
     sc.n_virtual = (uint32_t)v;
     sc.per = closed_group_size((uint32_t)n_bh, kBwdHeadGroup);  // a few units at a time stay in L2
     sc.ranks = (uint32_t)bwd_ranks(p.N);
-    sc.snake = 0;
     sc.n_ctas = (int)std::min<long long>(v, ctas_max);
     return true;
   }
@@ -849,32 +900,28 @@ int preview_bwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int
     std::copy(sc.item, sc.item + n, items);
     return n;
   }
-  // the closed form, walked exactly as the kernel's roles walk it
-  const ClosedSpec closed{sc.n_virtual, (uint32_t)p.B * (uint32_t)p.H, sc.per, sc.ranks, (uint32_t)sc.n_ctas,
-                          sc.snake};
+  // the queue: one list, in the order the CTAs take the tiles (the kernel's
+  // producer skips the ranks a sequence does not have)
+  const ClosedSpec order{sc.n_virtual, (uint32_t)p.B * (uint32_t)p.H, sc.per, sc.ranks, 1u, 0u};
   const int ranks = bwd_ranks(p.N);
   int n = 0;
-  for (int c = 0; c < sc.n_ctas; ++c) {
-    off[c] = n;
-    for (uint32_t k = 0;; ++k) {
-      const uint32_t f = closed_item(closed, (uint32_t)c, k);
-      if (f >= closed.n_virtual) break;
-      uint32_t uu, rr;
-      closed_unit_rank(closed, f, uu, rr);
-      const int r = (int)rr, u = (int)uu;
-      int len = p.N;
-      if (cu_host != nullptr) {
-        const int b = u / p.H, s0 = cu_host[b], s1 = cu_host[b + 1];
-        if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) continue;
-        len = s1 - s0;
-      }
-      const int kt = bwd_tile_of_rank(len, r);
-      if (kt < 0) continue;
-      if (n >= cap) return -2;
-      items[n++] = (uint32_t)((long long)u * ranks + kt);
+  for (uint32_t f = 0; f < sc.n_virtual; ++f) {
+    uint32_t uu, rr;
+    closed_unit_rank(order, f, uu, rr);
+    const int u = (int)uu;
+    int len = p.N;
+    if (cu_host != nullptr) {
+      const int b = u / p.H, s0 = cu_host[b], s1 = cu_host[b + 1];
+      if (s0 < 0 || s1 < s0 || s1 > p.T || s1 - s0 > p.N) continue;
+      len = s1 - s0;
     }
+    const int kt = bwd_tile_of_rank(len, (int)rr);
+    if (kt < 0) continue;
+    if (n >= cap) return -2;
+    items[n++] = (uint32_t)((long long)u * ranks + kt);
   }
-  off[sc.n_ctas] = n;
+  off[0] = 0;
+  for (int c = 1; c <= sc.n_ctas; ++c) off[c] = n;
   return n;
 }
 
@@ -893,6 +940,7 @@ cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   bp.dv = static_cast<__nv_bfloat16*>(p.dv);
   bp.cu = p.cu;
   bp.status = p.status;
+  bp.queue = p.queue;
   bp.limit_ns = p.wait_limit_ns;
   bp.B = p.B;
   bp.H = p.H;

@@ -102,8 +102,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
 /*
  * Bytes of device workspace fa_bwd needs: D_i (float32 per row) and, for the
- * tensor-core path, a float32 dQ accumulator of the shape of Q.  Pure host
- * arithmetic; never fails (returns 0 for invalid sizes).
+ * tensor-core path, a float32 dQ accumulator of the shape of Q and a 256-byte
+ * block holding the counter from which the backward's CTAs take key tiles
+ * (each part rounded up to 256 bytes).  Pure host arithmetic; never fails
+ * (returns 0 for invalid sizes).
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int D, const int32_t* cu_seqlens,
                              int total_tokens, fa_dtype dtype);
@@ -153,9 +155,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
  *     rejected with FA_ERR_WORKSPACE before anything is launched
  *     (fa_last_error_detail says why).  The workspace takes 4 * (D + 1)
  *     bytes per row (rows = B*H*N dense, H*total_tokens packed; each of its
- *     two parts rounded up to 256 bytes) for bf16 / fp16 and 4 bytes per row
- *     for float32, so 16 MiB holds at most 32,513 rows at D = 128, 64,527 rows
- *     at D = 64 and 4,194,304 rows in float32.
+ *     two parts rounded up to 256 bytes) plus 256 bytes for bf16 / fp16 and 4
+ *     bytes per row for float32, so 16 MiB holds at most 32,513 rows at
+ *     D = 128, 64,526 rows at D = 64 and 4,194,304 rows in float32.
  *   - Every call on a device shares the one array.  Its previous contents do
  *     not matter (the backward rewrites D_i and zeroes the dQ accumulator
  *     before reading them), but calls that overlap on the GPU -- on different
@@ -251,13 +253,15 @@ unsigned long long fa_launch_count(void);
  * *form): 0 = a table worked out on the host, for dense inputs of at most
  * 4096 items -- items in the order the one-CTA-per-item grid would hand them
  * out (heaviest first inside groups of heads), each to the CTA with the least
- * work so far, at most min(n_ctas, 160) CTAs; 1 = the closed-form list, for
- * larger or packed inputs -- units u = b * H + h cut into groups (the
- * backward: about 4 units each; the forward: one group), inside a group the
- * units' items rank-major, heaviest first, virtual item f counting the groups
- * one after the other; CTA c of n = min(n_ctas, B * H * ranks) takes
- * f = k * n + c (backward), or k * n + c for even k and k * n + n - 1 - c
- * for odd k (forward), skipping the ranks its sequence does not have.
+ * work so far, at most min(n_ctas, 160) CTAs; 1 = the forward's closed-form
+ * list, for larger or packed inputs -- unit u = b * H + h, the units' items
+ * rank-major (all units' heaviest first), CTA c of n = min(n_ctas,
+ * B * H * ranks) taking virtual item k * n + c for even k and
+ * k * n + n - 1 - c for odd k, skipping the ranks its sequence does not
+ * have; 2 = the backward's queue, for larger or packed inputs -- one list,
+ * in the order the CTAs take the tiles from a counter as they need them:
+ * units in groups of about 4, each group's tiles rank-major (off[0] = 0,
+ * off[i] = item count for i >= 1).
  * Item codes are u * R + pair (forward) or u * R + key tile (backward), with
  * R = ceil(ceil(N / 128) / 2) pairs or ceil(N / 128) key tiles.  Writes
  * off[0 .. c] (off must hold n_ctas + 1 entries; CTA i works on
@@ -300,8 +304,9 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
  * of adding per-key-tile partials into a float32 accumulator.  Costs three more
  * tile products per (query tile, key tile) pair.
  * Arguments as fa_bwd_dropout (p_drop = 0: no dropout).  workspace needs only
- * ceil(rows * 4 / 256) * 256 bytes (rows = B*H*N dense, H*total_tokens packed);
- * fa_bwd_workspace_size's larger value is accepted too.  float32 inputs run
+ * ceil(rows * 4 / 256) * 256 bytes (rows = B*H*N dense, H*total_tokens packed)
+ * plus 256 for bf16 / fp16; fa_bwd_workspace_size's larger value is accepted
+ * too.  float32 inputs run
  * the float32 path, which is deterministic already (FA_ERR_UNSUPPORTED if
  * p_drop > 0 there). */
 fa_status fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -187,11 +187,11 @@ def run_forward(pairs, seed, S=2, skip=()):
 
 
 
-def run_backward(items, seed, skip=()):
-    """items: list of step counts (one per key tile of this CTA).  The MMA
-    thread knows only how many tiles there are; each tile's step count reaches
-    it through a two-slot shared-memory ring the producer fills before arming
-    the tile's K / V barrier."""
+def run_backward(items, seed, skip=(), ring_slots=4):
+    """items: list of step counts (one per key tile of this CTA).  Only the
+    producer knows them: it hands each tile to the MMA thread and the compute
+    warps through a ring of records in shared memory (bar_item per slot,
+    bar_itemfree counting the three readers), then an end record."""
     rng = random.Random(seed)
     B = lambda n, c=1: Bar(n, c)
     kv = B("kv"); qf = [B("qf0", 2), B("qf1", 2)]; qe = [B("qe0"), B("qe1")]; of = B("of"); oe = B("oe")
@@ -207,7 +207,18 @@ def run_backward(items, seed, skip=()):
     tm = {"DP": None, "S": None, "acc": None}   # tensor-memory contents (what the last writer put there)
     drained = set()    # dQ steps read out of TMEM
     acc_read = set()   # items whose dK/dV the epilogue read out
-    steps_ring = [None, None]  # (tile, step count) per slot
+    R = ring_slots
+    ring = [None] * R          # (tile, step count) per slot; step count None = end
+    bitem = [B(f"item{s}") for s in range(R)]
+    bitemfree = [B(f"itemfree{s}", 3) for s in range(R)]   # MMA thread + two compute halves
+    def read_record(ii):
+        """generator: wait for tile ii's record, read it, free the slot; returns the step count"""
+        slot = ii % R
+        while not bitem[slot].try_wait((ii // R) & 1): yield
+        tag, n = ring[slot]
+        assert tag == ii, f"role reads the record of tile {tag} for tile {ii}"
+        bitemfree[slot].arrive()
+        return n
     def rd(k, d): reads[k] = reads.get(k, 0) + d
     def issue(op):
         pipe.append(op)
@@ -242,8 +253,14 @@ def run_backward(items, seed, skip=()):
     def producer():
         G = 0
         def load_kv(ii):
-            steps_ring[ii & 1] = (ii, items[ii])
             kv.arrive(tx=2); loads.append(("K", ii, kv, 1)); loads.append(("V", ii, kv, 1))
+        def publish(ii):
+            slot = ii % R
+            if ii >= R and "itemfree" not in skip:
+                while not bitemfree[slot].try_wait((ii // R - 1) & 1): yield
+            ring[slot] = (ii, items[ii] if ii < len(items) else None)
+            bitem[slot].arrive()
+        yield from publish(0)
         for ii, n in enumerate(items):
             if ii == 0: load_kv(0)
             for k in range(n):
@@ -262,12 +279,13 @@ def run_backward(items, seed, skip=()):
                     load_kv(ii)
                 yield
             G += n
+            yield from publish(ii + 1)
     def mma():
         G = 0
-        for ii in range(len(items)):
+        for ii in range(len(items) + 1):
+            n = yield from read_record(ii)
+            if n is None: return
             while not kv.try_wait(ii & 1): yield
-            tag, n = steps_ring[ii & 1]
-            assert tag == ii, f"MMA thread reads the step count of tile {tag} for tile {ii}"
             while not qf[G & 1].try_wait((G >> 1) & 1): yield
             issue(("S", {"g": G, "want": [ii, G]}, ["K", f"Q{G & 1}"])); issue(("commit", {"bar": bs, "want": []}, []))
             if G > 0:
@@ -314,7 +332,9 @@ def run_backward(items, seed, skip=()):
                 buf["stage"] = ("h1", gg); engine.append(("stage", ("h1", gg), stfree))
             staged[ch].arrive()
             yield
-        for ii, n in enumerate(items):
+        for ii in range(len(items) + 1):
+            n = yield from read_record(ii)
+            if n is None: return
             for k in range(n):
                 g = G + k
                 while not qf[g & 1].try_wait((g >> 1) & 1): yield

@@ -107,10 +107,11 @@ def test_backward_argument_validation(lib):
 
 def test_workspace_size(lib):
     f = lib.fa_bwd_workspace_size
-    # D vector (4 B per row) + float32 dQ accumulator for the tensor-core path
-    assert f(2, 32, 4096, 128, None, 0, 0) == 2 * 32 * 4096 * 4 + 2 * 32 * 4096 * 128 * 4
+    # D vector (4 B per row) + float32 dQ accumulator + a 256-byte block for the
+    # backward's tile counter, for the tensor-core path
+    assert f(2, 32, 4096, 128, None, 0, 0) == 2 * 32 * 4096 * 4 + 2 * 32 * 4096 * 128 * 4 + 256
     # packed: rows = H * T, rounded up to 256 bytes per part
-    assert f(16, 32, 8192, 128, 0x1000, 1001, 0) == (32 * 1001 * 4 + 255) // 256 * 256 + 32 * 1001 * 128 * 4
+    assert f(16, 32, 8192, 128, 0x1000, 1001, 0) == (32 * 1001 * 4 + 255) // 256 * 256 + 32 * 1001 * 128 * 4 + 256
     # fp16 uses the same tensor-core path and workspace as bf16
     assert f(2, 32, 4096, 128, None, 0, 2) == f(2, 32, 4096, 128, None, 0, 0)
     # float32 path needs only the D vector
@@ -191,11 +192,11 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 
 def test_static_scratch_limit(lib):
     """fa_bwd_static_ws's fixed scratch holds the workspace of at most 32,513
-    rows at D = 128, 64,527 at D = 64 and 4,194,304 in float32; one row more
+    rows at D = 128, 64,526 at D = 64 and 4,194,304 in float32; one row more
     needs more than FA_BWD_STATIC_WS_BYTES (refused before any launch)."""
     limit = 16 << 20
     size = lib.fa_bwd_workspace_size
-    for D, dt, rows in ((128, 0, 32513), (64, 0, 64527), (128, 2, 32513), (64, 1, 4194304)):
+    for D, dt, rows in ((128, 0, 32513), (64, 0, 64526), (128, 2, 32513), (64, 1, 4194304)):
         assert size(1, 1, rows, D, None, 0, dt) <= limit < size(1, 1, rows + 1, D, None, 0, dt)
         # the packed layout counts H * total_tokens rows
         assert size(3, 1, rows, D, 0x1000, rows, dt) <= limit < size(3, 1, rows, D, 0x1000, rows + 1, dt)
@@ -266,14 +267,12 @@ def test_persistent_table_covers_and_balances(lib, kernel, B, H, N, causal, ctas
 
 
 @pytest.mark.parametrize("kernel,B,H,N,causal", [
-    (1, 1, 32, 32768, 1),     # 8192 key tiles: the long-window backward
     (0, 1, 64, 32768, 1),     # 8192 pairs
-    (1, 4, 32, 8192, 0),      # 8192 key tiles, no mask
     (0, 3, 40, 12345, 1)])    # ragged length
 def test_persistent_closed_form_dense(lib, kernel, B, H, N, causal):
-    """Beyond 4096 items the closed form: every item once, heaviest ranks first
-    across all heads, a snake over the CTAs; for a list sorted by weight the
-    snake keeps every CTA within one item of the average."""
+    """Beyond 4096 items the forward's closed form: every item once, heaviest
+    ranks first across all heads, a snake over the CTAs; for a list sorted by
+    weight the snake keeps every CTA within one item of the average."""
     ctas = 152
     n, off, items, form = _preview(lib, kernel, B, H, N, causal, ctas)
     assert form == 1
@@ -288,13 +287,14 @@ def test_persistent_closed_form_dense(lib, kernel, B, H, N, causal):
     assert first // ranks == 0 and weight[first] == max(weight.values())
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("causal", [0, 1])
-def test_persistent_closed_form_packed(lib, kernel, causal):
-    """Packed sequences (the 16-sequence workload's seeded lengths): every
-    (sequence, head) item once, none of a sequence of length 0 or of a
-    malformed sequence, and every CTA within 10 % of the ideal finish time."""
+def test_persistent_closed_form_packed(lib, causal):
+    """Packed sequences in the forward (the 16-sequence workload's seeded
+    lengths): every (sequence, head) item once, none of a sequence of length
+    0 or of a malformed sequence, and every CTA within 10 % of the ideal
+    finish time."""
     from exact_io_aware_37_gb300 import synth
+    kernel = 0
     lengths = synth.varlen_lengths(16, 128, 8192).tolist()
     H, N = 32, max(lengths)
     n, off, items, form = _preview(lib, kernel, len(lengths), H, N, causal, 152, lengths=lengths)
@@ -311,8 +311,41 @@ def test_persistent_closed_form_packed(lib, kernel, causal):
     _loads(n2, off2, items2, weight2, used)
 
 
+@pytest.mark.parametrize("B,H,N,causal,lengths", [
+    (1, 32, 32768, 1, None),                 # 8192 key tiles: the long-window backward
+    (4, 32, 8192, 0, None),                  # no mask
+    (9, 7, 12345, 1, None),                  # ragged length, a short last group
+    (6, 3, 5000, 1, [300, 0, 5000, 129, 1, 4000]),
+    (16, 32, 8192, 1, "varlen16")])
+def test_backward_queue_order(lib, B, H, N, causal, lengths):
+    """Beyond the table (and for packed input) the backward's CTAs take key
+    tiles from one queue: every real tile exactly once; (sequence, head) units
+    in groups of about 4, each group's tiles contiguous and rank-major, so the
+    heaviest tiles of a group come first."""
+    if lengths == "varlen16":
+        from exact_io_aware_37_gb300 import synth
+        lengths = synth.varlen_lengths(16, 128, 8192).tolist()
+        N = max(lengths)
+    n, off, items, form = _preview(lib, 1, B, H, N, causal, 152, lengths=lengths)
+    assert form == 2
+    assert off[0] == 0 and all(o == n for o in off[1:])
+    weight = _weights(1, H, B, N, causal, lengths)
+    assert n == len(weight) and sorted(items) == sorted(weight)
+    ranks = (N + 127) // 128
+    units = [code // ranks for code in items]
+    tiles = [code % ranks for code in items]
+    n_units = B * H
+    per = -(-n_units // -(-n_units // 4))      # about 4 units per group, spread evenly
+    groups = [u // per for u in units]
+    assert groups == sorted(groups)          # one group after the other
+    for g in set(groups):
+        t = [kt for kt, gg in zip(tiles, groups) if gg == g]
+        assert t == sorted(t)                # rank-major: key tile 0 (the heaviest) of every unit first
+
+
 def test_persistent_schedule_refusals(lib):
     assert _preview(lib, 2, 1, 1, 128, 1, 152)[0] == -1         # no such kernel
     assert _preview(lib, 0, 1, 1, 0, 1, 152)[0] == -1           # empty problem
     assert _preview(lib, 1, 2, 32, 4096, 1, 152, cap=4)[0] == -2
     assert _preview(lib, 1, 1, 32, 32768, 1, 152, cap=100)[0] == -2
+    assert _preview(lib, 0, 1, 64, 32768, 1, 152, cap=100)[0] == -2

@@ -53,6 +53,24 @@ def test_backward_needs_every_wait(wait):
     pytest.fail(f"leaving out the {wait} wait went unnoticed")
 
 
+def test_backward_ring_needs_its_free_wait():
+    """The wait for a record slot's readers keeps the producer from overwriting
+    a record a role has not read: with a one-slot ring, leaving it out fails on
+    some run.  (The kernel's ring has four slots; the reducer, which this model
+    folds into the compute roles, can trail them by a step.)"""
+    for items, seed in _backward_cases():
+        try:
+            pm.run_backward(items, seed, skip=("itemfree",), ring_slots=1)
+        except AssertionError:
+            return
+    pytest.fail("leaving out the itemfree wait went unnoticed")
+
+
+def test_backward_ring_of_four_never_fails():
+    for items, seed in list(_backward_cases())[:500]:
+        assert pm.run_backward(items, seed, ring_slots=4)
+
+
 def test_backward_accumulator_release_is_implied():
     """The MMA thread's wait for the epilogue to have read the dK / dV
     accumulators is also implied by its wait for the next tile's P^T, which the
