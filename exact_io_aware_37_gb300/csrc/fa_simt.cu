@@ -234,24 +234,54 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(Problem p) {
 }
 
 // ---------------------------------------------------------------- preprocess
-// D_i = sum_d dO_id * O_id in fp32, one warp per row; optionally zeroes the
-// float32 dQ accumulator row.
-template <typename T>
+// D_i = sum_d dO_id * O_id in fp32; optionally zeroes the float32 dQ
+// accumulator row.  Each lane reads 16 bytes of O and of dO at a time, so a
+// row of D elements takes L = D * sizeof(T) / 16 lanes and a warp covers
+// 32 / L rows; the row sum is a butterfly over those L lanes.  The kernel is
+// a stream over O and dO (and the accumulator it zeroes): HBM-bound.
+template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(Problem p, long long rows, int zero_acc) {
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= rows) return;
-  const T* O = static_cast<const T*>(p.o);
-  const T* dO = static_cast<const T*>(p.dout);
+  constexpr int E = 16 / (int)sizeof(T);  // elements per 16-byte load
+  constexpr int L = D / E;                // lanes per row
+  static_assert(L >= 1 && L <= 32 && 32 % L == 0, "row split");
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = tid / L;
+  const int part = (int)(tid % L);
+  if (tid == 0 && p.queue != nullptr) *p.queue = 0u;  // the tensor-core backward's tile counter
+  const bool in = row < rows;
   float acc = 0.f;
-  for (int c = lane; c < p.D; c += 32) acc = fmaf(ld_elem(O, warp * p.D + c), ld_elem(dO, warp * p.D + c), acc);
+  if (in) {
+    const uint4 a = reinterpret_cast<const uint4*>(static_cast<const T*>(p.o) + row * D)[part];
+    const uint4 b = reinterpret_cast<const uint4*>(static_cast<const T*>(p.dout) + row * D)[part];
+    const T* ea = reinterpret_cast<const T*>(&a);
+    const T* eb = reinterpret_cast<const T*>(&b);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) p.dvec[warp] = acc;
-  if (warp == 0 && lane == 0 && p.queue != nullptr) *p.queue = 0u;  // the backward's tile counter
+    for (int e = 0; e < E; ++e) acc = fmaf(ld_elem(ea, e), ld_elem(eb, e), acc);
+  }
+#pragma unroll
+  for (int o = L / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (!in) return;
+  if (part == 0) p.dvec[row] = acc;
   if (zero_acc) {
-    float4* row = reinterpret_cast<float4*>(p.dq_acc + warp * p.D);
-    for (int c = lane; c < p.D / 4; c += 32) row[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* r = reinterpret_cast<float4*>(p.dq_acc + row * D);
+#pragma unroll
+    for (int c = part; c < D / 4; c += L) r[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+template <typename T>
+cudaError_t launch_preprocess_t(const Problem& p, long long rows, bool zero, cudaStream_t s) {
+  auto go = [&](auto kernel, int lanes_per_row) {
+    const long long threads = rows * lanes_per_row;
+    kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p, rows, zero ? 1 : 0);
+    return cudaGetLastError();
+  };
+  constexpr int E = 16 / (int)sizeof(T);
+  switch (p.D) {
+    case 32: return go(bwd_preprocess_kernel<T, 32>, 32 / E);
+    case 64: return go(bwd_preprocess_kernel<T, 64>, 64 / E);
+    case 128: return go(bwd_preprocess_kernel<T, 128>, 128 / E);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -310,15 +340,15 @@ cudaError_t launch_simt_bwd(const Problem& p, fa_dtype dt, cudaStream_t s) {
 cudaError_t launch_bwd_preprocess(const Problem& p, fa_dtype dt, bool zero_dq_acc, cudaStream_t s) {
   const long long rows = p.rows();
   if (rows == 0) return cudaSuccess;
-  const long long blocks = (rows * 32 + 255) / 256;
+  cudaError_t e;
   if (dt == FA_F32)
-    bwd_preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(p, rows, zero_dq_acc ? 1 : 0);
+    e = launch_preprocess_t<float>(p, rows, zero_dq_acc, s);
   else if (dt == FA_F16)
-    bwd_preprocess_kernel<__half><<<(unsigned)blocks, 256, 0, s>>>(p, rows, zero_dq_acc ? 1 : 0);
+    e = launch_preprocess_t<__half>(p, rows, zero_dq_acc, s);
   else
-    bwd_preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(p, rows, zero_dq_acc ? 1 : 0);
+    e = launch_preprocess_t<__nv_bfloat16>(p, rows, zero_dq_acc, s);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace fa

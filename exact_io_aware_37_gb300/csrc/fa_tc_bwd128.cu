@@ -55,7 +55,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int D = 128;
 constexpr int kTile = 128;  // keys per CTA and queries per step
 constexpr int kBwdHeadGroup = 4;  // heads per group of the causal block order: Q, dO and the dQ
                                    // accumulator of a head take 4 MB at N = 4096 (measured best of 2..32)
@@ -114,6 +113,7 @@ struct ItemRec {
 
 struct Bwd128Params {
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tdq;  // D = 64: the float32 dQ accumulator, for tensor reduce-adds
   DropParams drop;  // used by the dropout instantiation only
   const float* lse;
   const float* dvec;
@@ -131,29 +131,44 @@ struct Bwd128Params {
   BwdSched sched;
 };
 
-// Shared memory, dynamic only (1024-byte aligned base, checked).
-constexpr int kTileBytes = kTile * D * 2;  // 32 KB
-constexpr int kHalfBytes = kTile * 128;    // 16 KB: 64 columns of 128 rows
-constexpr int kKOff = 0;
-constexpr int kVOff = kTileBytes;
-constexpr int kQOff = 2 * kTileBytes;       // 2 stages
-constexpr int kDOOff = 4 * kTileBytes;      // 1 stage
-constexpr int kDSOff = 5 * kTileBytes;      // dS^T [128 keys][128 queries] bf16; dQ staging for queries 0-63
-constexpr int kStageOff = 6 * kTileBytes;   // dQ staging for queries 64-127: [64 queries][D] fp32
-constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
-constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
-constexpr int kBarOff = kDvOff + 1024;
+// Shared memory, dynamic only (1024-byte aligned base, checked), for head
+// width D (64 or 128).  A Q, K, V or dO tile is 128 rows of D elements in
+// D / 64 blocks of 64 columns (128 bytes, one 128-byte swizzle row).  The dQ
+// of a step leaves in two halves, each staged as one float32 box: at D = 128
+// dQ^T (head width on TMEM lanes) gives [64 queries][128] per query half; at
+// D = 64, dQ (queries on lanes) gives [128 queries][32] per head-width half.
+// Half 0 is staged in the dS^T buffer, free between dQ_k and dS^T_{k+1}.
+constexpr int kHalfBytes = kTile * 128;  // 16 KB: 64 columns of 128 rows
 constexpr int kNumBars = 20 + 2 * kItemRing;
-constexpr int kRingOff = kBarOff + kNumBars * 8;                    // kItemRing ItemRec
-constexpr int kMiscOff = kRingOff + kItemRing * (int)sizeof(ItemRec);
-constexpr int kSmemBytes = kMiscOff + 16;
-static_assert(kSmemBytes <= 232448, "shared-memory budget");
+template <int D>
+struct BwdLayout {
+  static constexpr int kTileBytes = kTile * D * 2;  // 32 KB or 16 KB; also one dQ half in float32
+  static constexpr int kHalves = D / 64;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;       // 2 stages
+  static constexpr int kDOOff = 4 * kTileBytes;      // 1 stage
+  static constexpr int kDSOff = 5 * kTileBytes;      // dS^T [128 keys][128 queries] bf16 (32 KB); dQ half 0
+  static constexpr int kStageOff = kDSOff + 32768;   // dQ half 1
+  static constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
+  static constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
+  static constexpr int kBarOff = kDvOff + 1024;
+  static constexpr int kRingOff = kBarOff + kNumBars * 8;  // kItemRing ItemRec
+  static constexpr int kMiscOff = kRingOff + kItemRing * (int)sizeof(ItemRec);
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static_assert(kSmemBytes <= 232448, "shared-memory budget");
+  static_assert(kDSOff % 1024 == 0 && kStageOff % 1024 == 0, "swizzled buffers need 1024-byte alignment");
+};
 
 // kDq = false: dK and dV only, for the deterministic backward (whose dQ comes
 // from the query-stationary kernel): no dS^T copy in shared memory, no dQ^T
 // product, read-out or reduction, and dP^T_k waits for nothing but dO_k.
-template <bool F16, bool kDrop, bool kDq>
+template <int D, bool F16, bool kDrop, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_constant__ Bwd128Params p) {
+  using C = BwdLayout<D>;
+  constexpr int kTileBytes = C::kTileBytes, kKOff = C::kKOff, kVOff = C::kVOff, kQOff = C::kQOff,
+                kDOOff = C::kDOOff, kDSOff = C::kDSOff, kStageOff = C::kStageOff, kLOff = C::kLOff,
+                kDvOff = C::kDvOff, kBarOff = C::kBarOff, kRingOff = C::kRingOff, kMiscOff = C::kMiscOff;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (smem_u32(smem) & 1023u) {  // the swizzled tile layout needs a 1024-byte aligned base
@@ -259,21 +274,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
     const int j = quad * 32 + lane;  // key row of S^T / dP^T; head-width column of dQ^T
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + ch * 64;
-    const uint32_t t_dp = tmem + lane_off + 128 + ch * 64;  // dP^T, dS^T, then dQ^T of this half
+    const uint32_t t_dp = tmem + lane_off + 128 + ch * 64;  // dP^T, dS^T, then (D = 128) dQ^T of this half
     uint8_t* ds_row = smem + kDSOff + ch * kHalfBytes + (j >> 3) * 1024 + (j & 7) * 128;
     float* stage = reinterpret_cast<float*>(smem + (ch == 0 ? kDSOff : kStageOff));
     bool ok = true;  // once a wait fails the rest are skipped (the abort flag is set)
 
-    // dQ^T of global step gg leaves tensor memory: this warp holds head-width
-    // column j for its half's 64 queries and writes them as rows [64 queries][D] fp32.
+    // dQ of global step gg leaves tensor memory.  D = 128: this warp holds
+    // head-width column j of dQ^T for its half's 64 queries and writes them as
+    // rows [64 queries][D] fp32.  D = 64: it holds query j's head-width
+    // columns [32 ch, 32 ch + 32) of dQ and writes them as row j of a
+    // [128 queries][32] fp32 box in the 128-byte swizzled layout the tensor
+    // reduce reads (16-byte chunk c of row j at chunk c ^ (j % 8): no two lanes
+    // of a quarter-warp write the same bank).
     auto drain_dq = [&](int gg) {
       ok = ok && warp_wait(bar_dq, gg & 1, w);
       tc_fence_after();
       uint32_t v[2][32];
-      tmem_ld32(t_dp, v[0]);
-      tmem_ld32(t_dp + 32, v[1]);
-      tmem_ld_wait(v[0]);
-      tmem_ld_wait(v[1]);
+      if constexpr (D == 128) {
+        tmem_ld32(t_dp, v[0]);
+        tmem_ld32(t_dp + 32, v[1]);
+        tmem_ld_wait(v[0]);
+        tmem_ld_wait(v[1]);
+      } else {
+        tmem_ld32(tmem + lane_off + 128 + ch * 32, v[0]);
+        tmem_ld_wait(v[0]);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
@@ -285,8 +310,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         ok = ok && warp_wait(bar_staged, gg & 1, w);
         if (gg > 0) ok = ok && warp_wait(bar_stfree, (gg - 1) & 1, w);
       }
+      if constexpr (D == 128) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) stage[e * D + j] = __uint_as_float(v[e >> 5][e & 31]);
+        for (int e = 0; e < 64; ++e) stage[e * D + j] = __uint_as_float(v[e >> 5][e & 31]);
+      } else {
+        uint8_t* row = reinterpret_cast<uint8_t*>(stage) + j * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(row + ((c ^ (j & 7)) << 4)) =
+              make_uint4(v[0][4 * c], v[0][4 * c + 1], v[0][4 * c + 2], v[0][4 * c + 3]);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_staged + ch);
@@ -415,15 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         const bool row_ok = key < len;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
-          __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + (it.out_base + key) * D + ch * 64;
+          __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + (it.out_base + key) * D + ch * (D / 2);
           const float mul = which == 0 ? 1.f : p.scale;
-          const uint32_t t_acc = tmem + lane_off + (which == 0 ? 256 : 384) + ch * 64;
+          const uint32_t t_acc = tmem + lane_off + (which == 0 ? 256 : 384) + ch * (D / 2);
 #pragma unroll 1
-          for (int c = 0; c < 64; c += 32) {
+          for (int c = 0; c < D / 2; c += 32) {
             uint32_t v[32];
             tmem_ld32(t_acc + c, v);
             tmem_ld_wait(v);
-            if (which == 1 && c == 32) {
+            if (which == 1 && c == D / 2 - 32) {
               // the accumulators are read: the next tile's dV / dK may start over them
               tc_fence_before();
               __syncwarp();
@@ -466,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           if (ii > 0) good = mbar_wait(bar_itemdone, (ii - 1) & 1, w);
           if (good) {
             mbar_arrive_expect_tx(bar_kv, 2 * kTileBytes);
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = 0; hf < C::kHalves; ++hf) {
               tma_load_3d(smem + kKOff + hf * kHalfBytes, &p.tk, bar_kv, hf * 64, it.row0 + it.kt * kTile, it.slab);
               tma_load_3d(smem + kVOff + hf * kHalfBytes, &p.tv, bar_kv, hf * 64, it.row0 + it.kt * kTile, it.slab);
             }
@@ -519,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
             mbar_arrive(bar_item + slot);  // releases the record to the roles' waits
             if (have && ii > 0)
               // its K and V wait for the previous tile's last products: have them in L2 by then
-              for (int hf = 0; hf < 2; ++hf) {
+              for (int hf = 0; hf < C::kHalves; ++hf) {
                 tma_prefetch_l2_3d(&p.tk, hf * 64, t.row0 + t.kt * kTile, t.slab);
                 tma_prefetch_l2_3d(&p.tv, hf * 64, t.row0 + t.kt * kTile, t.slab);
               }
@@ -564,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           }
           if (lane == 0) {
             mbar_arrive_expect_tx(bar_qf + st, kTileBytes);
-            for (int hf = 0; hf < 2; ++hf)
+            for (int hf = 0; hf < C::kHalves; ++hf)
               tma_load_3d(smem + kQOff + st * kTileBytes + hf * kHalfBytes, &p.tq, bar_qf + st, hf * 64,
                           it.row0 + qi * kTile, it.slab);
           }
@@ -580,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           }
           if (lane == 0) {
             mbar_arrive_expect_tx(bar_of, kTileBytes);
-            for (int hf = 0; hf < 2; ++hf)
+            for (int hf = 0; hf < C::kHalves; ++hf)
               tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, it.row0 + qi * kTile, it.slab);
           }
           o_issued = g + 1;
@@ -621,10 +654,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
               good = false;
               break;
             }
-            const int nq = min(64, it.len - (q0 + hf * 64));
-            if (nq > 0)
-              bulk_reduce_add_f32(p.dq_acc + (it.out_base + q0 + hf * 64) * D, smem + (hf == 0 ? kDSOff : kStageOff),
-                                  (uint32_t)nq * D * 4);
+            if constexpr (D == 128) {
+              // query half hf: rows of this sequence only
+              const int nq = min(64, it.len - (q0 + hf * 64));
+              if (nq > 0)
+                bulk_reduce_add_f32(p.dq_acc + (it.out_base + q0 + hf * 64) * D,
+                                    smem + (hf == 0 ? kDSOff : kStageOff), (uint32_t)nq * D * 4);
+            } else {
+              // head-width half hf of all 128 query rows: rows past the sequence
+              // hold zeros (their weights are zero) and rows past the tensor are
+              // clipped by the copy engine
+              tma_reduce_add_2d(&p.tdq, smem + (hf == 0 ? kDSOff : kStageOff), hf * 32, (int)(it.out_base + q0));
+            }
             bulk_commit();
           }
           if (!good || *abort_flag) {
@@ -643,7 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       // ---------------------------------------------------------- MMA issuer
       const uint32_t id_nn = idesc16<F16>(128, 128, false, false);  // S^T, dP^T: both K-major
       const uint32_t id_acc = idesc16<F16>(128, D, false, true);    // dV, dK: B MN-major
-      const uint32_t id_dq = idesc16<F16>(128, 128, true, true);    // dQ^T: both MN-major
+      // dQ^T = K^T dS^T (D = 128, M = head width) or dQ = dS K (D = 64, M = queries): both MN-major
+      const uint32_t id_dq = idesc16<F16>(128, D == 128 ? 128 : D, true, true);
       // Descriptors, advanced by adding (byte offset >> 4) to the start field.
       // k* = K-major view, m* = MN-major view of the same tile.
       const uint64_t kK = sdesc_sw128(smem_u32(smem + kKOff), 16, 1024);
@@ -660,23 +702,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       // Each group of 8 MMAs is issued back to back from one asm block.
       uint64_t a[8], b[8];
       uint32_t at[8];
-      auto issue_s = [&](int g) {  // S^T of global step g = K Q_g^T -> [0,128)
-        const int st = g & 1;
+      // D / 16 MMAs of K = 16 over the head width, back to back
+      auto issue_nn = [&](uint32_t d_tmem, uint64_t adesc, uint64_t bdesc) {
+        if constexpr (D == 128) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          a[ks] = kK + koff(ks);
-          b[ks] = kQ + st * kStageDesc + koff(ks);
+          for (int ks = 0; ks < 8; ++ks) {
+            a[ks] = adesc + koff(ks);
+            b[ks] = bdesc + koff(ks);
+          }
+          mma_ss_x8(d_tmem, a, b, id_nn, 0u);
+        } else {
+          uint64_t a4[4], b4[4];
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            a4[ks] = adesc + koff(ks);
+            b4[ks] = bdesc + koff(ks);
+          }
+          mma_ss_x4(d_tmem, a4, b4, id_nn, 0u);
         }
-        mma_ss_x8(tmem + 0, a, b, id_nn, 0u);
+      };
+      auto issue_s = [&](int g) {  // S^T of global step g = K Q_g^T -> [0,128)
+        issue_nn(tmem + 0, kK, kQ + (g & 1) * kStageDesc);
         mma_commit(bar_s);
       };
       auto issue_dp = [&]() {  // dP^T = V dO^T -> [128,256)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          a[ks] = kV + koff(ks);
-          b[ks] = kDO + koff(ks);
-        }
-        mma_ss_x8(tmem + 128, a, b, id_nn, 0u);
+        issue_nn(tmem + 128, kV, kDO);
         mma_commit(bar_dp);
       };
       bool ok = true;
@@ -755,10 +805,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           mma_ts_x8(tmem + 384, at, b, id_acc, acc0);
           mma_commit(bar_qe + st);
           if constexpr (kDq) {
+            // D = 128: dQ^T = K^T dS^T; D = 64: dQ = dS K (the same two MN-major
+            // views, as A and B the other way round) -> [128, 128 + D or 128)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              a[ks] = mK + moff(ks);
-              b[ks] = mDS + moff(ks);
+              a[ks] = (D == 128 ? mK : mDS) + moff(ks);
+              b[ks] = (D == 128 ? mDS : mK) + moff(ks);
             }
             mma_ss_x8(tmem + 128, a, b, id_dq, 0u);
             mma_commit(bar_dq);
@@ -925,14 +977,21 @@ int preview_bwd_schedule(const Problem& p, const int32_t* cu_host, int ctas, int
   return n;
 }
 
-template <bool F16, bool kDrop, bool kDq>
+template <int D, bool F16, bool kDrop, bool kDq>
 cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
+  using C = BwdLayout<D>;
   static Bwd128Params bp;  // large (the schedule); filled in full below on every call
   static std::mutex launch_mu;
   std::lock_guard<std::mutex> launch_lock(launch_mu);
   if (!make_map16(&bp.tq, p.q, p, kTile) || !make_map16(&bp.tk, p.k, p, kTile) ||
       !make_map16(&bp.tv, p.v, p, kTile) || !make_map16(&bp.tdo, p.dout, p, kTile))
     return note_error("backward tensor map encode", cudaErrorInvalidValue);
+  if constexpr (D == 64 && kDq) {
+    // the tensor reduce addresses accumulator rows with 32-bit coordinates
+    if (p.rows() > 0x7fffffffll) return note_error("backward: more than 2^31 rows at D = 64", cudaErrorInvalidValue);
+    if (!make_map_acc32(&bp.tdq, p.dq_acc, (uint64_t)p.rows(), D))
+      return note_error("backward dQ accumulator tensor map encode", cudaErrorInvalidValue);
+  }
   bp.lse = p.lse;
   bp.dvec = p.dvec;
   bp.dq_acc = p.dq_acc;
@@ -950,22 +1009,33 @@ cudaError_t launch_bwd128_t(const Problem& p, cudaStream_t s) {
   bp.scale = p.scale;
   bp.causal = p.causal;
   bp.drop = drop_params_of(p);
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<F16, kDrop, kDq>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd128_kernel<D, F16, kDrop, kDq>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return note_error("backward smem attribute", e);
-  if (!build_sched(p, bp.sched)) return note_error("backward schedule (no multiprocessor count, or more than 2^31 work items)", cudaErrorInvalidValue);
-  tc_bwd128_kernel<F16, kDrop, kDq><<<bp.sched.n_ctas, kThreads, kSmemBytes, s>>>(bp);
+  if (!build_sched(p, bp.sched))
+    return note_error("backward schedule (no multiprocessor count, or more than 2^31 work items)",
+                      cudaErrorInvalidValue);
+  tc_bwd128_kernel<D, F16, kDrop, kDq><<<bp.sched.n_ctas, kThreads, C::kSmemBytes, s>>>(bp);
   note_launches(1);
   return note_error("backward launch", cudaGetLastError());
 }
 
+template <int D, bool kDq>
+cudaError_t launch_bwd_dispatch(const Problem& p, cudaStream_t s) {
+  if (p.dropout) return p.f16 ? launch_bwd128_t<D, true, true, kDq>(p, s) : launch_bwd128_t<D, false, true, kDq>(p, s);
+  return p.f16 ? launch_bwd128_t<D, true, false, kDq>(p, s) : launch_bwd128_t<D, false, false, kDq>(p, s);
+}
+
 cudaError_t launch_tc_bwd128(const Problem& p, cudaStream_t s) {
-  if (p.dropout) return p.f16 ? launch_bwd128_t<true, true, true>(p, s) : launch_bwd128_t<false, true, true>(p, s);
-  return p.f16 ? launch_bwd128_t<true, false, true>(p, s) : launch_bwd128_t<false, false, true>(p, s);
+  if (p.D == 64) return launch_bwd_dispatch<64, true>(p, s);
+  if (p.D == 128) return launch_bwd_dispatch<128, true>(p, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tc_bwd128_dkdv(const Problem& p, cudaStream_t s) {
-  if (p.dropout) return p.f16 ? launch_bwd128_t<true, true, false>(p, s) : launch_bwd128_t<false, true, false>(p, s);
-  return p.f16 ? launch_bwd128_t<true, false, false>(p, s) : launch_bwd128_t<false, false, false>(p, s);
+  if (p.D == 64) return launch_bwd_dispatch<64, false>(p, s);
+  if (p.D == 128) return launch_bwd_dispatch<128, false>(p, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

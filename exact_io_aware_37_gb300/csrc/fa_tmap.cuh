@@ -46,4 +46,20 @@ inline bool make_map16(CUtensorMap* map, const void* base, const Problem& p, int
   return r == CUDA_SUCCESS;
 }
 
+// The float32 dQ accumulator [rows, D] as a 2-D array (D, rows) for tensor
+// reduce-adds of boxes of 32 columns (128 bytes, one 128-byte swizzle row) x
+// 128 rows, read from shared memory in the 128-byte swizzled layout.
+inline bool make_map_acc32(CUtensorMap* map, float* base, uint64_t rows, int D) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa

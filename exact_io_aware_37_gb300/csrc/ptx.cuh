@@ -173,6 +173,16 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
+// 2-D tiled reduce-add of one box from shared memory into global memory
+// (float32 add by the copy engine, tracked in the issuing thread's bulk groups
+// like bulk_reduce_add_f32).  c0 is the innermost coordinate (its byte offset
+// must be a multiple of 16); rows past the tensor's end are not written.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src, int c0, int c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's committed bulk groups still read shared memory.
 template <int N>
