@@ -41,9 +41,8 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 # kernel from one ncu capture, keyed by the SHA-256 of that kernel's source
 # file at capture time (reported as null once the source has changed).
 TRAFFIC_BY_SOURCE = {
-    # tc_bwd128_kernel<bf16>, B2 H32 N4096 D128 causal: 404.9 MB read + 218.9 MB written
-    # (captured at source 4ebcd99a...; this source differs from it in comments and host code only)
-    "ec7921e537e77216f7a3ce7ad93fd411fa19d9b6bac844aab867bf4a100b81bb": 623.8e6,
+    # tc_bwd128_kernel<128, bf16>, B2 H32 N4096 D128 causal: 404.9 MB read + 218.6 MB written
+    "d1226cf71b0a92876863361374e86d11b66c8f1bc3cfb74d137189c4ceaa2c19": 623.5e6,
     # decode_split_kernel, B16 H32 nq1 nk8192 D128: 2147.7 MB read + 3.9 MB written
     "690b84cb5610de6d23e66e577f0baf49ac3373182539be7030411dc3bd37a5e8": 2151.6e6,
 }
@@ -384,9 +383,9 @@ def main():
     # dominant kernel: the main backward kernel (2.5x the forward FLOPs), timed
     # by events the library records right around it
     dom_ms = statistics.mean(main_ms)
-    dom_name = "tc_bwd128_kernel" if path == "tcgen05" else "simt backward kernels"
+    dom_name = "tc_bwd128_kernel<128>" if path == "tcgen05" else "simt backward kernels"
     if args.deterministic:
-        dom_name = "tc_bwd_kernel (dK, dV) + tc_bwd_dq_kernel (dQ)"
+        dom_name = "tc_bwd128_kernel (dK, dV) + tc_bwd_dq_kernel (dQ)"
     src = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc",
                        "fa_tc_bwd128.cu" if path == "tcgen05" else "fa_simt.cu")
     # the ncu capture behind the table was of the bf16 run
@@ -539,7 +538,7 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
     peak_tf, _, peak_kind = peaks()
     value = world * 3.5 * f_fwd / (ms_step * 1e-3) / 1e12
     bwd_main_tf = 2.5 * f_fwd / (ms_main * 1e-3) / 1e12
-    kernel = "tc_bwd128_kernel" if D == 128 else "tc_bwd_kernel<64>"
+    kernel = f"tc_bwd128_kernel<{D}>"
     if rank != 0:
         return
     line = {
