@@ -403,13 +403,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
 
         ok = ok && warp_wait(bar_dp, g & 1, w);
         tc_fence_after();
-        tmem_ld32(t_dp, sv[0]);
-        tmem_ld32(t_dp + 32, sv[1]);
-        tmem_ld_wait(sv[0]);
-        tmem_ld_wait(sv[1]);
+        if constexpr (!kDrop) {
+          tmem_ld32(t_dp, sv[0]);
+          tmem_ld32(t_dp + 32, sv[1]);
+          tmem_ld_wait(sv[0]);
+          tmem_ld_wait(sv[1]);
+        }
         uint32_t dsp[32];
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
+          if constexpr (kDrop) {
+            // one 32-column half of dP^T at a time (the generator's work leaves no
+            // registers for both at once)
+            if (c8 % 4 == 0) {
+              tmem_ld32(t_dp + 32 * (c8 / 4), sv[c8 / 4]);
+              tmem_ld_wait(sv[c8 / 4]);
+            }
+          }
           const float4 da = sd4[2 * c8], db = sd4[2 * c8 + 1];
           const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
 #pragma unroll

@@ -176,3 +176,29 @@ def test_empty_inputs():
     o, lse = fa.forward(q, q, q, causal=True, cu_seqlens=cu, max_seqlen=1)
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_error() == 0
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_dense_beyond_the_table(D, causal):
+    """Dense inputs with more than 4096 items: the forward walks its closed-form
+    list (4608 query-tile pairs) and the backward takes key tiles from the
+    workspace queue (9216 tiles), unlike the smaller cases above, which use the
+    host-built table.  Sampled heads against the oracle, the gradient sums of
+    every head (rows of P sum to one, rows of dS to zero)."""
+    B, H, N = 8, 64, 2300
+    q, k, v, do = synth.qkv_do((B, H, N, D), torch.bfloat16, seed_offset=300)
+    scale = default_scale(D)
+    got = run(q, k, v, do, causal, scale)
+    g = np.random.default_rng(11)
+    for idx in sorted(g.choice(B * H, size=6, replace=False).tolist()):
+        b, h = divmod(idx, H)
+        qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
+        O, L = oracle.forward_head(qn, kn, vn, scale, causal)
+        dQ, dK, dV, _ = oracle.backward_head(qn, kn, vn, don, scale, causal)
+        compare(torch.bfloat16, {n: f64(t[b, h]) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+                f"beyond the table D={D} causal={causal} head {(b, h)}")
+    dk, dv = got["dk"].float(), got["dv"].float()
+    assert ((dk.sum(-2).abs() / dk.abs().sum(-2).clamp_min(1e-6)).max().item()) < 2e-2
+    dod = do.to(dv.device).float()
+    assert (((dv.sum(-2) - dod.sum(-2)).abs() / dod.abs().sum(-2).clamp_min(1e-6)).max().item()) < 2e-2
