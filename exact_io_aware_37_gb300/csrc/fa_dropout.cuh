@@ -49,31 +49,35 @@ __device__ __forceinline__ uint32_t keep4(const DropParams& d, uint32_t i, uint3
   return (w.x >= d.thr ? 1u : 0u) | (w.y >= d.thr ? 2u : 0u) | (w.z >= d.thr ? 4u : 0u) | (w.w >= d.thr ? 8u : 0u);
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& w, uint32_t t) {
-  return t == 0 ? w.x : t == 1 ? w.y : t == 2 ? w.z : w.w;
-}
-
 // Keep bits (bit c for query q0 + c, c < 64) of this thread's key `key` when
 // keys sit on the lanes of a warp and lanes 4m .. 4m+3 hold keys 4m' .. 4m'+3
 // (key = 4 * (key / 4) + lane % 4).  The four lanes sharing key / 4 need the
 // four words of the same generator call for each query, so each of them
-// computes the calls for a quarter of the queries (q = q0 + 4g + lane % 4)
-// and the words are exchanged within the quad: in round r lane t receives,
-// from lane (t + r) mod 4, that lane's word t.  All 32 lanes must call this.
+// computes the calls for a quarter of the queries (q = q0 + 4g + lane % 4):
+// call g's four decisions (bit k: key 4 * (key / 4) + k) form nibble g of a
+// 64-bit word, and the quad exchanges whole words -- lane t takes bit t of
+// every nibble of lane s's word, which is the decision for its key at query
+// q0 + 4g + s.  Four pairs of shuffles and a few shifts per 64 decisions, no
+// per-decision selects or variable shifts.  All 32 lanes must call this.
 __device__ __forceinline__ uint64_t keep64_keys_on_lanes(const DropParams& d, uint32_t key, uint32_t q0,
                                                          uint32_t bh, int lane) {
   const uint32_t t = lane & 3;
-  const uint32_t quad_base = lane & ~3;
-  uint64_t bits = 0;
+  const int quad_base = lane & ~3;
+  uint64_t nibs = 0;  // nibble g at bits 4g .. 4g + 3
 #pragma unroll 4
   for (int g = 0; g < 16; ++g) {
     const uint4 w = philox4x32_10(make_uint4(key >> 2, q0 + 4 * g + t, bh, d.offset), d);
+    const uint32_t nib = (w.x >= d.thr ? 1u : 0u) | (w.y >= d.thr ? 2u : 0u) | (w.z >= d.thr ? 4u : 0u) |
+                         (w.w >= d.thr ? 8u : 0u);
+    nibs |= (uint64_t)nib << (4 * g);
+  }
+  const uint32_t lo = (uint32_t)nibs, hi = (uint32_t)(nibs >> 32);
+  uint64_t bits = 0;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const uint32_t send = word_of(w, (t - r) & 3);  // this lane's word for lane (t - r) mod 4
-      const uint32_t got = __shfl_sync(0xffffffffu, send, quad_base | ((t + r) & 3));
-      if (got >= d.thr) bits |= 1ull << (4 * g + ((t + r) & 3));
-    }
+  for (int s = 0; s < 4; ++s) {
+    const uint64_t word = (uint64_t)__shfl_sync(0xffffffffu, hi, quad_base | s) << 32 |
+                          __shfl_sync(0xffffffffu, lo, quad_base | s);
+    bits |= ((word >> t) & 0x1111111111111111ull) << s;
   }
   return bits;
 }

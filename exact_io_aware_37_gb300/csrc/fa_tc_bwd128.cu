@@ -347,9 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         const float4* sd4 = reinterpret_cast<const float4*>(s_d + st * 128 + ch * 64);
         // dropout decisions of (this half's 64 queries, this key), regenerated
         uint64_t keepm = ~0ull;
-        if constexpr (kDrop)
+        if constexpr (kDrop) {
           keepm = keep64_keys_on_lanes(p.drop, (uint32_t)key, (uint32_t)(qi * kTile + ch * 64), (uint32_t)(b * p.H + h),
                                        lane);
+          // formed here, before the waits, where the previous step's values are dead
+          asm volatile("" : "+l"(keepm));
+        }
         ok = ok && warp_wait(bar_qf + st, (g >> 1) & 1, w) && warp_wait(bar_s, g & 1, w);
         tc_fence_after();
         uint32_t sv[2][32];
