@@ -84,8 +84,14 @@ struct DecodeArgs {
 };
 
 // Rows g0 .. g0 + G - 1 of the queries (those >= nq are skipped).
+// Blocks per SM the register budget must allow: the one-row kernel is a pure
+// stream and wants as many loads in flight as it can get; eight rows of state
+// need the registers of one 256-thread block per SM.
+template <int G, int D>
+constexpr int dec_min_blocks() { return G == 1 ? (D == 64 ? 6 : 4) : G == 4 ? 2 : 1; }
+
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecThreads, dec_min_blocks<G, D>()) decode_split_kernel(const DecodeArgs a) {
   constexpr int E = D / 32;
   __shared__ float s_m[kDecWarps][G], s_l[kDecWarps][G];
   __shared__ float s_u[kDecWarps][G][D];

@@ -397,6 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           tmem_st32(t_s, pk);
           tmem_st_wait();
         }
+        if constexpr (kDrop) {
+          // the keep decisions ride in the sign bits of the weights from here on
+          // (every weight is >= 0; a dropped one becomes -P, a masked 0 -0), so the
+          // mask's registers are free before the dQ read-out below
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            pr[c] = __uint_as_float(__float_as_uint(pr[c]) | ((~(uint32_t)(keepm >> c) & 1u) << 31));
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_p);
@@ -429,13 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           for (int e = 0; e < 4; ++e) {
             const int c = c8 * 8 + 2 * e;
             float t0, t1, d0, d1;  // dS = P o (dP - D), two columns per packed op
-            float dp0 = __uint_as_float(sv[c >> 5][c & 31]), dp1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
-            if constexpr (kDrop) {  // dP of the dropped weights: masked and scaled like them
-              dp0 = (keepm >> c) & 1 ? dp0 * p.drop.scale : 0.f;
-              dp1 = (keepm >> (c + 1)) & 1 ? dp1 * p.drop.scale : 0.f;
+            const float dp0 = __uint_as_float(sv[c >> 5][c & 31]), dp1 = __uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]);
+            if constexpr (kDrop) {
+              // dP of the dropped weights is masked and scaled like them: with w = +-P
+              // (sign = dropped), dS = max(w, 0) * scale * dP - |w| * D
+              d0 = fmaf(fmaxf(pr[c], 0.f) * p.drop.scale, dp0, -fabsf(pr[c]) * dv[2 * e]);
+              d1 = fmaf(fmaxf(pr[c + 1], 0.f) * p.drop.scale, dp1, -fabsf(pr[c + 1]) * dv[2 * e + 1]);
+            } else {
+              fsub2(t0, t1, dp0, dp1, dv[2 * e], dv[2 * e + 1]);
+              fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
             }
-            fsub2(t0, t1, dp0, dp1, dv[2 * e], dv[2 * e + 1]);
-            fmul2(d0, d1, pr[c], pr[c + 1], t0, t1);
             dsp[4 * c8 + e] = pack16x2<F16>(d0, d1);
           }
         }

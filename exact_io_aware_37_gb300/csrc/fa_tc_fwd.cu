@@ -256,6 +256,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         float l = 0.f;
         for (int j = 0; j < n; ++j) {
           const int g = G + j;
+          // dropout: the tile's keep decisions (bit k of kw[x]: key j * kBN + 32 x + k)
+          // depend on positions alone, so they are drawn before S is ready: 32
+          // independent generator calls the warp interleaves while the MMA runs
+          // (eight calls a pass; the passes rotate their words through kw, so no
+          // index is dynamic)
+          uint32_t kw[4] = {0u, 0u, 0u, 0u};
+          if constexpr (kDrop) {
+            const uint32_t bh = (uint32_t)(q.b * p.H + q.h);
+#pragma unroll 1
+            for (int x = 0; x < 4; ++x) {
+              uint32_t word = 0;
+#pragma unroll
+              for (int gk = 0; gk < 8; ++gk)
+                word |= keep4(p.drop, (uint32_t)i, (uint32_t)(j * kBN + 32 * x + 4 * gk), bh) << (4 * gk);
+              kw[0] = kw[1];
+              kw[1] = kw[2];
+              kw[2] = kw[3];
+              kw[3] = word;
+            }
+          }
           if (!warp_wait(&bar_s[t], cs & 1, w)) {
             ok = false;
             break;
@@ -303,13 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           const float nmu = (m_ref == -INFINITY) ? 0.f : -m_ref;
           // p = 2^(s * scale * log2(e) - m_ref), two columns per packed FMA
           float rs0 = 0.f, rs1 = 0.f;
-          uint32_t kbits = 0;
+          // P goes to tensor memory in parts of kPer packed columns (quarters with
+          // dropout, whose keep words take registers the halves would need)
+          constexpr int kParts = kDrop ? 4 : 2, kPer = kBN / 2 / kParts;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t pk[32];
+          for (int hf = 0; hf < kParts; ++hf) {
+            uint32_t pk[kPer];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int e0 = 64 * hf + 2 * c;
+            for (int c = 0; c < kPer; ++c) {
+              const int e0 = 2 * kPer * hf + 2 * c;
               float a0, a1;
               ffma2(a0, a1, __uint_as_float(sr[e0 >> 5][e0 & 31]), __uint_as_float(sr[(e0 + 1) >> 5][(e0 + 1) & 31]),
                     p.c2, nmu, nmu);
@@ -317,17 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
               const float p1 = ex2_approx(a1);
               fadd2(rs0, rs1, p0, p1);  // the normaliser is that of the undropped weights
               if constexpr (kDrop) {
-                // dropped weights enter PV scaled by 1 / (1 - p); one generator call per 4 keys
-                if ((c & 1) == 0)
-                  kbits = keep4(p.drop, (uint32_t)i, (uint32_t)(k0 + e0), (uint32_t)(q.b * p.H + q.h));
-                const uint32_t sh = (c & 1) * 2;
-                pk[c] = pack16x2<F16>((kbits >> sh) & 1u ? p0 * p.drop.scale : 0.f,
-                                      (kbits >> (sh + 1)) & 1u ? p1 * p.drop.scale : 0.f);
+                // dropped weights enter PV scaled by 1 / (1 - p)
+                const uint32_t kb = kw[e0 >> 5] >> (e0 & 31);
+                pk[c] = pack16x2<F16>(kb & 1u ? p0 * p.drop.scale : 0.f, kb & 2u ? p1 * p.drop.scale : 0.f);
               } else {
                 pk[c] = pack16x2<F16>(p0, p1);
               }
             }
-            tmem_st32(t_s + 32 * hf, pk);
+            if constexpr (kPer == 32)
+              tmem_st32(t_s + 32 * hf, pk);
+            else
+              tmem_st16(t_s + 16 * hf, pk);
           }
           l += rs0 + rs1;
           if (j > 0 && __any_sync(0xffffffffu, grow)) {
