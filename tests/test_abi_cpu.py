@@ -190,6 +190,25 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
                          None) == CUDA
 
 
+def test_no_kernel_spills_registers(lib):
+    """ptxas's report of every translation unit the library is built from: no
+    kernel stores registers to local memory (a spill in a role of a
+    warp-specialised kernel puts local-memory round trips on its critical path)."""
+    spills = []
+    for src in fa_build.SOURCES:
+        log = os.path.join(fa_build.BUILD, src.replace(".cu", ".ptxas.txt"))
+        assert os.path.exists(log), f"no ptxas report for {src}"
+        kernel = None
+        for line in open(log):
+            m = re.search(r"Compiling entry function '(\S+)'", line)
+            if m:
+                kernel = m.group(1)
+            m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+            if m and (int(m.group(1)) or int(m.group(2))):
+                spills.append((src, kernel, line.strip()))
+    assert not spills, spills
+
+
 def test_static_scratch_limit(lib):
     """fa_bwd_static_ws's fixed scratch holds the workspace of at most 32,513
     rows at D = 128, 64,526 at D = 64 and 4,194,304 in float32; one row more
