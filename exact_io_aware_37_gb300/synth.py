@@ -4,7 +4,9 @@ This module holds no attention arithmetic: only random-number recipes and the
 workload shapes.  Every tensor is drawn in fp32 on the CPU from its own
 ``torch.Generator`` seed and then rounded to the dtype the kernels read, so the
 oracle (which upcasts the same rounded values to float64) and the GPU path see
-identical inputs.
+identical inputs.  Tensors too large to draw on the host (the size-limit test)
+are drawn by the same recipe on the device (``normal_device``); the oracle
+then reads the rows it checks back from there.
 
 Seeds: Q=0, K=1, V=2, dO=3, variable-length sequence lengths=4.
 """
@@ -23,6 +25,21 @@ def normal(shape, seed, dtype, std=1.0):
     if std != 1.0:
         x.mul_(std)
     return x.to(dtype)
+
+
+def normal_device(shape, seed, dtype, device, std=1.0):
+    """i.i.d. N(0, std^2) in fp32 on ``device`` from ``seed``, rounded to
+    ``dtype``; drawn one slice of the leading dimensions at a time (every slice
+    in order from the same generator), so the fp32 temporary stays small."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    out = torch.empty(tuple(shape), dtype=dtype, device=device)
+    flat = out.view(-1, shape[-2], shape[-1])
+    for i in range(flat.shape[0]):
+        x = torch.randn((shape[-2], shape[-1]), generator=g, dtype=torch.float32, device=device)
+        if std != 1.0:
+            x.mul_(std)
+        flat[i].copy_(x)
+    return out
 
 
 def qkv_do(shape, dtype, std=1.0, seed_offset=0):

@@ -120,3 +120,36 @@ def test_varlen16_h32d128_causal():
     dQ, dK, dV, _ = oracle.backward_varlen(qn, kn, vn, don, cu, scale, True)
     compare(torch.bfloat16, {n: f64(t[heads]) for n, t in got.items()},
             dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV), "varlen sampled heads")
+
+
+def test_beyond_32_bit_element_offsets():
+    """B1 H72 N262144 D128 causal bf16: 2.4e9 elements (4.8 GB) per tensor and a
+    9.7 GB float32 dQ accumulator, so element and byte offsets pass 2^31 and
+    2^32; the forward walks its closed-form list (73,728 query-tile pairs) and
+    the backward its queue (147,456 key tiles).  Every head: finite outputs and
+    the gradient sums; sampled rows, among them the last rows of the last head
+    (the largest offsets), against the oracle."""
+    import exact_io_aware_37_gb300 as fa
+    B, H, N, D = 1, 72, 262144, 128
+    assert B * H * N * D > 2 ** 31
+    dev = torch.device("cuda:0")
+    q, k, v, do = (synth.normal_device((B, H, N, D), 500 + s, torch.bfloat16, dev, std=0.5) for s in range(4))
+    scale = default_scale(D)
+    o, lse = fa.forward(q, k, v, causal=True)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
+    for h in range(H):
+        got = dict(o=o[:, h], lse=lse[:, h], dq=dq[:, h], dk=dk[:, h], dv=dv[:, h])
+        for t in got.values():
+            assert torch.isfinite(t).all(), f"head {h}"
+        _invariants(got, do[:, h])
+    tol = TOL[torch.bfloat16]
+    for h in (0, 35, H - 1):
+        rows = sorted(set([0, 1, 127, 128, N // 2, N - 129, N - 2, N - 1] + _sample(N, 4, 2000 + h)))
+        qn, kn, vn, don = (x[0, h].double().cpu().numpy() for x in (q, k, v, do))
+        O, L = oracle.forward_rows(qn, kn, vn, rows, scale, True)
+        assert np.abs(f64(o[0, h, rows]) - O).max() <= tol["o_max"], f"O head {h}"
+        assert np.abs(f64(lse[0, h, rows]) - L).max() <= tol["lse_max"], f"L head {h}"
+        dQ = oracle.backward_dq_rows(qn, kn, vn, don, rows, scale, True)
+        assert rel_frob(f64(dq[0, h, rows]), dQ) <= tol["grad_rel"], f"dQ head {h}"
