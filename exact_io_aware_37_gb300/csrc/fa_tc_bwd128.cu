@@ -62,6 +62,12 @@ constexpr int kThreads = 384;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kReduceWarp = 10;
+// D = 128: half 0 of a step's dQ is staged and reduced as two 16 KB pieces
+// (query rows 0-31 and 32-63), each of which overlays one query half of the
+// dS^T buffer, so the copy engine starts on the first piece while the second is
+// still being written, and each half of the next dS^T waits only for its own
+// piece to be read.
+constexpr bool kH0Pieces = true;
 // setmaxnreg split of the kLaunchRegs budget: the MMA issuer keeps five groups of
 // eight descriptors in flight and needs more than the forward's support share
 constexpr int kBwdComputeRegs = 184;
@@ -139,7 +145,9 @@ struct Bwd128Params {
 // D = 64, dQ (queries on lanes) gives [128 queries][32] per head-width half.
 // Half 0 is staged in the dS^T buffer, free between dQ_k and dS^T_{k+1}.
 constexpr int kHalfBytes = kTile * 128;  // 16 KB: 64 columns of 128 rows
-constexpr int kNumBars = 20 + 2 * kItemRing;
+// (the two barriers of half 0's second piece exist at D = 128 only)
+template <int D>
+constexpr int num_bars() { return 20 + 2 * kItemRing + (D == 128 && kH0Pieces ? 2 : 0); }
 template <int D>
 struct BwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;  // 32 KB or 16 KB; also one dQ half in float32
@@ -153,6 +161,7 @@ struct BwdLayout {
   static constexpr int kLOff = kStageOff + kTileBytes;  // 2 x 128 floats: L * log2(e)
   static constexpr int kDvOff = kLOff + 1024;           // 2 x 128 floats: D
   static constexpr int kBarOff = kDvOff + 1024;
+  static constexpr int kNumBars = num_bars<D>();
   static constexpr int kRingOff = kBarOff + kNumBars * 8;  // kItemRing ItemRec
   static constexpr int kMiscOff = kRingOff + kItemRing * (int)sizeof(ItemRec);
   static constexpr int kSmemBytes = kMiscOff + 16;
@@ -195,6 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   uint64_t* bar_accfree = bars + 19;  // dK / dV of a key tile read out of TMEM (8 compute warps)
   uint64_t* bar_item = bars + 20;     // [kItemRing] a tile's record written (producer)
   uint64_t* bar_itemfree = bars + 20 + kItemRing;  // [kItemRing] record read (every consumer role)
+  // D = 128 with kH0Pieces: bar_staged[0] / bar_dsfree cover half 0's first piece
+  // (and the first query half of the dS^T buffer), these two its second piece
+  constexpr bool kPieces = D == 128 && kH0Pieces;
+  uint64_t* bar_staged0b = kPieces ? bars + 20 + 2 * kItemRing : nullptr;  // half 0's second piece staged (4 warps)
+  uint64_t* bar_dsfree1 = kPieces ? bars + 21 + 2 * kItemRing : nullptr;   // second query half of the dS^T buffer read
   ItemRec* ring = reinterpret_cast<ItemRec*>(smem + kRingOff);
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   int* abort_flag = reinterpret_cast<int*>(smem + kMiscOff + 4);
@@ -242,10 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
   if (table && n_table <= 0) return;  // (a table gives every CTA of the launch work)
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
+    for (int i = 0; i < C::kNumBars; ++i) {
       uint64_t* bar = bars + i;
       const bool by8 = bar == bar_p || bar == bar_ds || bar == bar_dqfree || bar == bar_accfree;
-      const bool by4 = bar == bar_staged || bar == bar_staged + 1;
+      const bool by4 = bar == bar_staged || bar == bar_staged + 1 || bar == bar_staged0b;
       const bool by2 = bar == bar_qf || bar == bar_qf + 1;  // Q bytes + L / D written
       // a record is read by the 8 compute warps, the MMA issuer and the reducer
       const bool readers = bar >= bar_itemfree && bar < bar_itemfree + kItemRing;
@@ -307,8 +321,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
       if (ch == 1) {
         // half 0 goes to the copy engine first and its buffer gates the next dS^T:
         // let its warps have the shared-memory write bandwidth to themselves
-        ok = ok && warp_wait(bar_staged, gg & 1, w);
+        ok = ok && warp_wait(kPieces ? bar_staged0b : bar_staged, gg & 1, w);
         if (gg > 0) ok = ok && warp_wait(bar_stfree, (gg - 1) & 1, w);
+      }
+      if constexpr (kPieces) {
+        if (ch == 0) {
+          // rows 0-31, published, then rows 32-63: two pieces for the copy engine
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stage[e * D + j] = __uint_as_float(v[0][e]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_staged);
+#pragma unroll
+          for (int e = 32; e < 64; ++e) stage[e * D + j] = __uint_as_float(v[1][e - 32]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_staged0b);
+          return;
+        }
       }
       if constexpr (D == 128) {
 #pragma unroll
@@ -453,7 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         tmem_st32(t_dp, dsp);  // dS^T as bf16 pairs over this half's first 32 dP^T columns (already read)
         if constexpr (kDq) {
           // the dS^T buffer held half 0 of the previous dQ until the copy engine read it
-          if (g > 0) ok = ok && warp_wait(bar_dsfree, (g - 1) & 1, w);
+          // (with the two pieces, each query half waits for its own piece)
+          if (g > 0)
+            ok = ok && warp_wait((kPieces && ch == 1) ? bar_dsfree1 : bar_dsfree, (g - 1) & 1, w);
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8)  // 128-byte swizzle: 16-byte chunk c8 of row j sits at chunk c8 ^ (j % 8)
             *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (j & 7)) << 4)) =
@@ -673,6 +705,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         for (int kk = 0; good && kk < it.n_steps; ++kk) {
           const int gg = G + kk;
           const int q0 = (it.q_first + kk) * kTile;
+          if constexpr (kPieces) {
+            // half 0 as two 32-row pieces from the dS^T buffer, then half 1
+            for (int pc = 0; pc < 3; ++pc) {
+              uint64_t* bar = pc == 0 ? bar_staged : pc == 1 ? bar_staged0b : bar_staged + 1;
+              if (!mbar_wait(bar, gg & 1, w)) {
+                good = false;
+                break;
+              }
+              const int r0 = pc == 2 ? 64 : pc * 32;  // first query row of the piece: 0, 32, 64
+              const int nq = min(pc == 2 ? 64 : 32, it.len - (q0 + r0));
+              if (nq > 0)
+                bulk_reduce_add_f32(p.dq_acc + (it.out_base + q0 + r0) * D,
+                                    smem + (pc == 2 ? kStageOff : kDSOff + pc * 16384), (uint32_t)nq * D * 4);
+              bulk_commit();
+            }
+            if (!good || *abort_flag) {
+              good = false;
+              break;
+            }
+            bulk_wait_read<2>();  // rows 0-31 read: the first query half of the dS^T buffer
+            mbar_arrive(bar_dsfree);
+            bulk_wait_read<1>();  // rows 32-63 read: the second
+            mbar_arrive(bar_dsfree1);
+            bulk_wait_read<0>();  // half 1 read
+            mbar_arrive(bar_stfree);
+            continue;
+          }
           for (int hf = 0; hf < 2; ++hf) {
             if (!mbar_wait(bar_staged + hf, gg & 1, w)) {
               good = false;

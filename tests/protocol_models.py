@@ -187,19 +187,27 @@ def run_forward(pairs, seed, S=2, skip=()):
 
 
 
-def run_backward(items, seed, skip=(), ring_slots=4):
+def run_backward(items, seed, skip=(), ring_slots=4, pieces=False):
     """items: list of step counts (one per key tile of this CTA).  Only the
     producer knows them: it hands each tile to the MMA thread and the compute
     warps through a ring of records in shared memory (bar_item per slot,
-    bar_itemfree counting the three readers), then an end record."""
+    bar_itemfree counting the three readers), then an end record.
+    pieces: the head-width-128 scheme, in which the dS^T buffer is two query
+    halves and half 0 of dQ goes to the copy engine as two pieces, each staged
+    over one of them and each releasing its own half (bar_dsfree / bar_dsfree1);
+    half 1 is staged after the second piece.  Otherwise (head width 64) half 0
+    is one piece over the whole buffer."""
     rng = random.Random(seed)
     B = lambda n, c=1: Bar(n, c)
     kv = B("kv"); qf = [B("qf0", 2), B("qf1", 2)]; qe = [B("qe0"), B("qe1")]; of = B("of"); oe = B("oe")
     bs = B("s"); dp = B("dp"); bp = B("p", 2); ds = B("ds", 2); dq = B("dq"); dqfree = B("dqfree", 2)
     dsfree = B("dsfree"); staged = [B("staged0"), B("staged1")]; stfree = B("stfree")
+    staged0b = B("staged0b"); dsfree1 = B("dsfree1")
+    DS = ["dSa", "dSb"] if pieces else ["dS"]   # the dS^T buffer: two query halves, or one
     itemdone = B("itemdone"); accfree = B("accfree", 2)
     G0 = [sum(items[:i]) for i in range(len(items))]
-    buf = {"K": None, "V": None, "Q0": None, "Q1": None, "dO": None, "dS": None, "stage": None}
+    buf = {"K": None, "V": None, "Q0": None, "Q1": None, "dO": None, "dS": None, "dSa": None, "dSb": None,
+           "stage": None}
     reads = {}
     loads = []
     pipe = []
@@ -310,7 +318,7 @@ def run_backward(items, seed, skip=(), ring_slots=4):
                     issue(("S", {"g": g + 1, "want": [ii, g + 1]}, ["K", f"Q{st ^ 1}"])); issue(("commit", {"bar": bs, "want": []}, []))
                 while not ds.try_wait(g & 1): yield
                 issue(("dK", {"g": g, "acc0": k > 0, "item": ii, "want": [g]}, [f"Q{st}"])); issue(("commit", {"bar": qe[st], "want": []}, []))
-                issue(("dQ", {"g": g, "want": [ii, ("dS", g)]}, ["K", "dS"])); issue(("commit", {"bar": dq, "want": []}, []))
+                issue(("dQ", {"g": g, "want": [ii] + [("dS", g)] * len(DS)}, ["K"] + DS)); issue(("commit", {"bar": dq, "want": []}, []))
                 yield
             issue(("commit", {"bar": itemdone, "want": []}, []))
             G += n
@@ -321,10 +329,17 @@ def run_backward(items, seed, skip=(), ring_slots=4):
             drained.add(gg); dqfree.arrive()   # (each half arrives; count 2)
             yield
             if ch == 1:
-                while not staged[0].try_wait(gg & 1): yield
+                while not (staged0b if pieces else staged[0]).try_wait(gg & 1): yield
                 if gg > 0:
                     if "stfree" not in skip:
                         while not stfree.try_wait((gg - 1) & 1): yield
+            if ch == 0 and pieces:
+                for half, bar_st, bar_free in (("dSa", staged[0], dsfree), ("dSb", staged0b, dsfree1)):
+                    assert reads.get(half, 0) == 0, "staging over dS while dQ still reads it"
+                    buf[half] = ("h0", gg); engine.append((half, ("h0", gg), bar_free))
+                    bar_st.arrive()
+                    yield
+                return
             if ch == 0:
                 assert reads.get("dS", 0) == 0, "staging over dS while dQ still reads it"
                 buf["dS"] = ("h0", gg); engine.append(("dS", ("h0", gg), dsfree))
@@ -347,8 +362,13 @@ def run_backward(items, seed, skip=(), ring_slots=4):
                 assert tm["DP"] == ("dP", g), f"compute {ch} step {g} sees {tm['DP']}"
                 if g > 0:
                     if "dsfree" not in skip:
-                        while not dsfree.try_wait((g - 1) & 1): yield
-                if ch == 0: buf["dS"] = ("dS", g)   # both halves write; model the buffer's content once
+                        while not (dsfree1 if pieces and ch == 1 else dsfree).try_wait((g - 1) & 1): yield
+                if pieces:
+                    half = DS[ch]
+                    assert reads.get(half, 0) == 0, "dS^T written while dQ still reads it"
+                    buf[half] = ("dS", g)
+                elif ch == 0:
+                    buf["dS"] = ("dS", g)   # both halves write; model the buffer's content once
                 ds.arrive()
                 yield
             yield from drain(G + n - 1)

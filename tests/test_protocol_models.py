@@ -28,9 +28,10 @@ def test_forward_protocol_never_fails():
         assert pm.run_forward(pairs, seed, stages)
 
 
-def test_backward_protocol_never_fails():
+@pytest.mark.parametrize("pieces", [False, True], ids=["one_piece", "two_pieces"])
+def test_backward_protocol_never_fails(pieces):
     for items, seed in _backward_cases():
-        assert pm.run_backward(items, seed)
+        assert pm.run_backward(items, seed, pieces=pieces)
 
 
 @pytest.mark.parametrize("wait", ["epi", "qfree", "vfree", "kfree"])
@@ -43,11 +44,12 @@ def test_forward_needs_every_wait(wait):
     pytest.fail(f"leaving out the {wait} wait went unnoticed")
 
 
+@pytest.mark.parametrize("pieces", [False, True], ids=["one_piece", "two_pieces"])
 @pytest.mark.parametrize("wait", ["itemdone", "dsfree", "stfree", "dqfree_first"])
-def test_backward_needs_every_wait(wait):
+def test_backward_needs_every_wait(wait, pieces):
     for items, seed in _backward_cases():
         try:
-            pm.run_backward(items, seed, skip=(wait,))
+            pm.run_backward(items, seed, skip=(wait,), pieces=pieces)
         except AssertionError:
             return
     pytest.fail(f"leaving out the {wait} wait went unnoticed")
