@@ -132,3 +132,31 @@ def test_zero_probability_is_plain_attention():
     assert np.array_equal(got["o"], f64(o)) and np.array_equal(got["lse"], f64(lse))
     for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         assert np.abs(got[n] - f64(t)).max() <= 1e-2   # dQ's float32 accumulation order is not fixed
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_dropout_beyond_the_table(D):
+    """More items than the host-built table holds (the forward's closed-form list
+    of 4608 query-tile pairs, the backward's queue of 9216 key tiles): every
+    role derives a tile's head from the list, and the decisions regenerated from
+    that head must still be the oracle's.  Sampled heads against the oracle."""
+    B, H, N, p, seed, off = 8, 64, 2300, 0.1, 4242, 3
+    q, k, v, do = synth.qkv_do((B, H, N, D), torch.bfloat16, seed_offset=310)
+    scale = default_scale(D)
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    o, lse = torch.empty_like(qd), torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    fa.fa_fwd_dropout(qd, kd, vd, o, lse, True, p, seed, off, scale)
+    fa.fa_bwd_dropout(qd, kd, vd, o, lse, dod, dq, dk, dv, True, p, seed, off, scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
+    got = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+    g = np.random.default_rng(13)
+    for idx in sorted(g.choice(B * H, size=3, replace=False).tolist()):
+        b, h = divmod(idx, H)
+        qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
+        keep = oracle.dropout_keep(N, N, b * H + h, _p32(p), seed, off)
+        O, L = oracle.forward_head_dropout(qn, kn, vn, scale, True, _p32(p), keep)
+        dQ, dK, dV, _ = oracle.backward_head_dropout(qn, kn, vn, don, scale, True, _p32(p), keep)
+        compare(torch.bfloat16, {n: f64(t[b, h]) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+                f"dropout beyond the table D={D} head {(b, h)}", o_scale=1.0 / (1.0 - p))
