@@ -101,3 +101,34 @@ def test_repeated_calls_are_bit_identical():
         b = _run(q, k, v, do, True, default_scale(128))
         for n in ("dq", "dk", "dv"):
             assert np.array_equal(a[n], b[n]), n
+
+
+def test_deterministic_beyond_the_table():
+    """Dense input with more key tiles (9216) than the host-built table holds:
+    the dK / dV kernel takes them from the workspace queue.  Sampled heads
+    against the oracle, and a second call bit-identical to the first."""
+    B, H, N, D = 8, 64, 2300, 128
+    q, k, v, do = synth.qkv_do((B, H, N, D), torch.bfloat16, seed_offset=320)
+    scale = default_scale(D)
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    o, lse = torch.empty_like(qd), torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    fa.fa_fwd(qd, kd, vd, o, lse, True, scale)
+    runs = []
+    for _ in range(2):
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+        fa.fa_bwd_deterministic(qd, kd, vd, o, lse, dod, dq, dk, dv, True, scale)
+        torch.cuda.synchronize()
+        assert fa.fa_get_last_device_error() == 0
+        runs.append((dq, dk, dv))
+    for a, b in zip(*runs):
+        assert torch.equal(a, b), "repeated deterministic backward differs"
+    dq, dk, dv = runs[0]
+    got = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+    g = np.random.default_rng(17)
+    for idx in sorted(g.choice(B * H, size=3, replace=False).tolist()):
+        b, h = divmod(idx, H)
+        qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
+        O, L = oracle.forward_head(qn, kn, vn, scale, True)
+        dQ, dK, dV, _ = oracle.backward_head(qn, kn, vn, don, scale, True)
+        compare(torch.bfloat16, {n: f64(t[b, h]) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+                f"deterministic beyond the table head {(b, h)}")
