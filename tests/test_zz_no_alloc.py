@@ -57,6 +57,31 @@ def test_two_calls_in_a_row_match_fa_bwd():
     _check(got, ref, torch.bfloat16)
 
 
+def test_packed_sequences_match_the_oracle():
+    """Packed sequences: their backward always takes key tiles from the queue,
+    whose counter then lives in the fixed scratch too.  Checked against the
+    oracle itself, not against fa_bwd."""
+    import oracle
+    dev = torch.device("cuda:0")
+    lengths = [700, 1, 0, 383, 1290]
+    cu = synth.cu_seqlens(lengths)
+    H, T, D = 3, int(cu[-1]), 128
+    q, k, v, do = synth.qkv_do((H, T, D), torch.bfloat16, seed_offset=83)
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
+    cud, scale = cu.to(dev), 1.0 / D ** 0.5
+    o, lse = fa.forward(qd, kd, vd, causal=True, scale=scale, cu_seqlens=cud, max_seqlen=max(lengths))
+    got = [torch.full_like(qd, float("nan")) for _ in range(3)]
+    fa.fa_bwd_static_ws(qd, kd, vd, o, lse, dod, *got, True, scale, cud, max(lengths))
+    torch.cuda.synchronize()
+    assert fa.fa_get_last_device_error() == 0
+    qn, kn, vn, don = (x.double().numpy() for x in (q, k, v, do))
+    dQ, dK, dV, _ = oracle.backward_varlen(qn, kn, vn, don, cu, scale, True)
+    for g, r, name in zip(got, (dQ, dK, dV), ("dq", "dk", "dv")):
+        gn = g.double().cpu().numpy()
+        assert np.isfinite(gn).all(), name
+        assert rel_frob(gn, r) <= TOL[torch.bfloat16]["grad_rel"], name
+
+
 def test_float32_path_matches_fa_bwd():
     got, ref = _both_ways((1, 2, 200, 64), torch.float32, True, seed_offset=82)
     _check(got, ref, torch.float32)
