@@ -178,16 +178,18 @@ def test_empty_inputs():
     assert fa.fa_get_last_device_error() == 0
 
 
-@pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
-def test_dense_beyond_the_table(D, causal):
+@pytest.mark.parametrize("D, causal, dtype", [(64, False, torch.bfloat16), (64, True, torch.bfloat16),
+                                              (128, False, torch.bfloat16), (128, True, torch.bfloat16),
+                                              (128, True, torch.float16)],
+                         ids=lambda x: str(x).split(".")[-1])
+def test_dense_beyond_the_table(D, causal, dtype):
     """Dense inputs with more than 4096 items: the forward walks its closed-form
     list (4608 query-tile pairs) and the backward takes key tiles from the
     workspace queue (9216 tiles), unlike the smaller cases above, which use the
     host-built table.  Sampled heads against the oracle, the gradient sums of
     every head (rows of P sum to one, rows of dS to zero)."""
     B, H, N = 8, 64, 2300
-    q, k, v, do = synth.qkv_do((B, H, N, D), torch.bfloat16, seed_offset=300)
+    q, k, v, do = synth.qkv_do((B, H, N, D), dtype, seed_offset=300)
     scale = default_scale(D)
     got = run(q, k, v, do, causal, scale)
     g = np.random.default_rng(11)
@@ -196,8 +198,8 @@ def test_dense_beyond_the_table(D, causal):
         qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
         O, L = oracle.forward_head(qn, kn, vn, scale, causal)
         dQ, dK, dV, _ = oracle.backward_head(qn, kn, vn, don, scale, causal)
-        compare(torch.bfloat16, {n: f64(t[b, h]) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
-                f"beyond the table D={D} causal={causal} head {(b, h)}")
+        compare(dtype, {n: f64(t[b, h]) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+                f"beyond the table D={D} causal={causal} {dtype} head {(b, h)}")
     dk, dv = got["dk"].float(), got["dv"].float()
     assert ((dk.sum(-2).abs() / dk.abs().sum(-2).clamp_min(1e-6)).max().item()) < 2e-2
     dod = do.to(dv.device).float()
