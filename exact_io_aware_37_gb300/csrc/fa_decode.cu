@@ -35,39 +35,60 @@ constexpr int kKeysPerIter = 4;
 constexpr int kDecodeMaxG = 8;  // query rows per CTA (static shared memory: 8 warps x 8 rows x 128 floats)
 
 template <typename T, int E>
-struct RowLoad;  // E (even) consecutive elements of a row, as float
+struct RowLoad;  // E (even) consecutive elements of a row, as float, in the widest aligned loads
 template <int E>
 struct RowLoad<float, E> {
   static __device__ __forceinline__ void load(const float* p, float (&x)[E]) {
+    if constexpr (E % 4 == 0) {  // 16-byte loads (a lane's E elements start E * 4 bytes into a 16-byte aligned row)
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const float2 t = *reinterpret_cast<const float2*>(p + e);
-      x[e] = t.x;
-      x[e + 1] = t.y;
+      for (int e = 0; e < E; e += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p + e);
+        x[e] = t.x;
+        x[e + 1] = t.y;
+        x[e + 2] = t.z;
+        x[e + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        const float2 t = *reinterpret_cast<const float2*>(p + e);
+        x[e] = t.x;
+        x[e + 1] = t.y;
+      }
     }
   }
 };
-template <int E>
-struct RowLoad<__nv_bfloat16, E> {
-  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[E]) {
+// 16-bit types: four elements per 8-byte load where E allows it
+template <typename T2, typename T, int E>
+__device__ __forceinline__ void load16(const T* p, float (&x)[E]) {
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < E; e += 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p + e);
+      const T2 a = *reinterpret_cast<const T2*>(&u.x), b = *reinterpret_cast<const T2*>(&u.y);
+      x[e] = __low2float(a);
+      x[e + 1] = __high2float(a);
+      x[e + 2] = __low2float(b);
+      x[e + 3] = __high2float(b);
+    }
+  } else {
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
-      const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(p + e);
+      const T2 t = *reinterpret_cast<const T2*>(p + e);
       x[e] = __low2float(t);
       x[e + 1] = __high2float(t);
     }
+  }
+}
+template <int E>
+struct RowLoad<__nv_bfloat16, E> {
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&x)[E]) {
+    load16<__nv_bfloat162>(p, x);
   }
 };
 template <int E>
 struct RowLoad<__half, E> {
-  static __device__ __forceinline__ void load(const __half* p, float (&x)[E]) {
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      const __half2 t = *reinterpret_cast<const __half2*>(p + e);
-      x[e] = __low2float(t);
-      x[e + 1] = __high2float(t);
-    }
-  }
+  static __device__ __forceinline__ void load(const __half* p, float (&x)[E]) { load16<__half2>(p, x); }
 };
 
 struct DecodeArgs {
