@@ -145,6 +145,32 @@ struct Bwd128Params {
 // D = 64, dQ (queries on lanes) gives [128 queries][32] per head-width half.
 // Half 0 is staged in the dS^T buffer, free between dQ_k and dS^T_{k+1}.
 constexpr int kHalfBytes = kTile * 128;  // 16 KB: 64 columns of 128 rows
+
+// Transpose of 16-byte chunks within each group of E consecutive lanes (E a
+// power of two): on entry chunk slot s of lane g + b (g the group's first lane)
+// holds chunk s of row b; on return slot s holds chunk b of row s.  One xor
+// step per bit swaps that bit between the lane and the slot index.
+template <int E>
+__device__ __forceinline__ void exchange_chunks(uint32_t (&u)[4 * E], int lane) {
+#pragma unroll
+  for (int m = E / 2; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int s0 = 0; s0 < E; ++s0) {
+      if (s0 & m) continue;
+      const int s1 = s0 | m;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        // the lower lane keeps slot s0 and passes slot s1 up; the upper the reverse
+        const uint32_t send = hi ? u[4 * s0 + q] : u[4 * s1 + q];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        u[4 * s0 + q] = hi ? recv : u[4 * s0 + q];
+        u[4 * s1 + q] = hi ? u[4 * s1 + q] : recv;
+      }
+    }
+  }
+}
+
 // (the two barriers of half 0's second piece exist at D = 128 only)
 template <int D>
 constexpr int num_bars() { return 20 + 2 * kItemRing + (D == 128 && kH0Pieces ? 2 : 0); }
@@ -498,38 +524,46 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         if (lane == 0) mbar_arrive(bar_ds);
       }
       if constexpr (kDq) drain_dq(G + it.n_steps - 1);
-      // epilogue: dV and dK rows of this tile's keys, once its last products are complete
+      // epilogue: dV and dK rows of this tile's keys, once its last products are complete.
+      // Both are read out of tensor memory and packed first, so the accumulators are
+      // handed back before any store; each thread then holds E 16-byte chunks of its
+      // own key row, which an E x E exchange within groups of E lanes turns into whole
+      // rows per store instruction (32 / E rows of a full 128-byte line each, instead
+      // of one line per lane).
       if (ok && warp_wait(bar_itemdone, ii & 1, w)) {
         tc_fence_after();
-        const bool row_ok = key < len;
-#pragma unroll 1
+        constexpr int E = D / 16;  // 16-byte chunks in this half's D / 2 columns
+        uint32_t pk[2][4 * E];     // dV, dK of key row j, columns ch * D / 2 .., as 16-bit pairs
+#pragma unroll
         for (int which = 0; which < 2; ++which) {
-          __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + (it.out_base + key) * D + ch * (D / 2);
           const float mul = which == 0 ? 1.f : p.scale;
           const uint32_t t_acc = tmem + lane_off + (which == 0 ? 256 : 384) + ch * (D / 2);
-#pragma unroll 1
+#pragma unroll
           for (int c = 0; c < D / 2; c += 32) {
             uint32_t v[32];
             tmem_ld32(t_acc + c, v);
             tmem_ld_wait(v);
-            if (which == 1 && c == D / 2 - 32) {
-              // the accumulators are read: the next tile's dV / dK may start over them
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_accfree);
-            }
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                uint4 u;
-                u.x = pack16x2<F16>(__uint_as_float(v[8 * v4 + 0]) * mul, __uint_as_float(v[8 * v4 + 1]) * mul);
-                u.y = pack16x2<F16>(__uint_as_float(v[8 * v4 + 2]) * mul, __uint_as_float(v[8 * v4 + 3]) * mul);
-                u.z = pack16x2<F16>(__uint_as_float(v[8 * v4 + 4]) * mul, __uint_as_float(v[8 * v4 + 5]) * mul);
-                u.w = pack16x2<F16>(__uint_as_float(v[8 * v4 + 6]) * mul, __uint_as_float(v[8 * v4 + 7]) * mul);
-                dst[v4] = u;
-              }
-            }
+            for (int e = 0; e < 16; ++e)
+              pk[which][c / 2 + e] = pack16x2<F16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          }
+        }
+        // the accumulators are read: the next tile's dV / dK may start over them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_accfree);
+        const int grp = lane & ~(E - 1), sub = lane & (E - 1);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          exchange_chunks<E>(pk[which], lane);
+          // chunk slot i now holds chunk `sub` of key row grp + i of this warp's 32
+          __nv_bfloat16* out = (which == 0 ? p.dv : p.dk) + ch * (D / 2) + sub * 8;
+#pragma unroll
+          for (int i = 0; i < E; ++i) {
+            const int r = it.kt * kTile + quad * 32 + grp + i;
+            if (r < len)
+              *reinterpret_cast<uint4*>(out + (it.out_base + r) * D) =
+                  make_uint4(pk[which][4 * i], pk[which][4 * i + 1], pk[which][4 * i + 2], pk[which][4 * i + 3]);
           }
         }
       }
