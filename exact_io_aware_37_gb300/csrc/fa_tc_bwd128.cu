@@ -654,6 +654,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
         if (state > 0) it = ring[slot];
         return state;
       };
+      // L and D rows of a step (rows past the sequence's end read its last row and
+      // are stored as zero).  A tile's first step fetches its own; every later
+      // step's are fetched a step ahead, so the loads are in flight while the
+      // producer waits for buffers instead of holding up the next Q copy.
+      float lv[4], dv[4];
+      auto fetch_ld = [&](const ItemRec& t, int q) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const long long row = t.out_base + min(q * kTile + lane * 4 + e, t.len - 1);
+          lv[e] = p.lse[row];
+          dv[e] = p.dvec[row];
+        }
+      };
       ItemRec it;
       int state = next_tile(0, it);
       if (state < 0) good_all = false;
@@ -669,17 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
           // Q / L / D stage st was last used by step g - 2 (free once its dK has
           // completed); the single dO buffer by step g - 1 (free once its dV has).
           // Lane 0 waits and the answer is broadcast, so the warp never splits.
-          // L and D of the tile are fetched before the wait, so the Q copy goes out
-          // as soon as its stage is free; the stage's barrier takes a second
-          // arrival once they are in shared memory.
-          float lv[4], dv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int qrow = qi * kTile + lane * 4 + e;
-            const bool in = qrow < it.len;
-            lv[e] = in ? p.lse[it.out_base + qrow] * kLog2e : 0.f;
-            dv[e] = in ? p.dvec[it.out_base + qrow] : 0.f;
-          }
+          // The stage's barrier takes a second arrival once L and D are in shared
+          // memory.
+          if (k == 0) fetch_ld(it, qi);
           if (lane == 0 && g >= 2) good = mbar_wait(bar_qe + st, ((g >> 1) - 1) & 1, w);
           if (!__shfl_sync(0xffffffffu, good, 0)) {
             good_all = false;
@@ -692,8 +697,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
                           it.row0 + qi * kTile, it.slab);
           }
           q_issued = g + 1;
-          *reinterpret_cast<float4*>(s_l + st * 128 + lane * 4) = make_float4(lv[0], lv[1], lv[2], lv[3]);
-          *reinterpret_cast<float4*>(s_d + st * 128 + lane * 4) = make_float4(dv[0], dv[1], dv[2], dv[3]);
+          {  // L and D into the stage, then its barrier's second arrival
+            float l4[4], d4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool in = qi * kTile + lane * 4 + e < it.len;
+              l4[e] = in ? lv[e] * kLog2e : 0.f;
+              d4[e] = in ? dv[e] : 0.f;
+            }
+            *reinterpret_cast<float4*>(s_l + st * 128 + lane * 4) = make_float4(l4[0], l4[1], l4[2], l4[3]);
+            *reinterpret_cast<float4*>(s_d + st * 128 + lane * 4) = make_float4(d4[0], d4[1], d4[2], d4[3]);
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_qf + st);
           if (lane == 0 && g >= 1) good = mbar_wait(bar_oe, (g - 1) & 1, w);
@@ -707,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd128_kernel(const __grid_con
               tma_load_3d(smem + kDOOff + hf * kHalfBytes, &p.tdo, bar_of, hf * 64, it.row0 + qi * kTile, it.slab);
           }
           o_issued = g + 1;
+          if (k + 1 < it.n_steps) fetch_ld(it, qi + 1);
           if (k == 0 && ii > 0 && !load_kv(it, ii)) {
             good_all = false;
             break;
