@@ -306,12 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
               for (int e = 0; e < 32; ++e)
                 if (c * 32 + e >= kmax) sr[c][e] = __float_as_uint(-INFINITY);
           }
-          // row maximum of the raw scores (scale > 0 preserves the order)
-          float mt = -INFINITY;
+          // row maximum of the raw scores (scale > 0 preserves the order), as eight
+          // independent partial maxima so that the exponentials wait for a chain of
+          // 11 dependent steps instead of 64 (the maximum is exact in any order)
+          float mp[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) mp[r] = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) mt = fmax3(mt, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+            for (int e = 0; e < 32; e += 2)
+              mp[(e >> 1) & 7] = fmax3(mp[(e >> 1) & 7], __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+          const float mt = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7]));
           const float m_new = fmaxf(m_ref, mt * p.c2);
           float alpha = 1.f;
           const bool grow = m_new > m_ref + kRescaleThreshold;
