@@ -146,31 +146,6 @@ struct Bwd128Params {
 // Half 0 is staged in the dS^T buffer, free between dQ_k and dS^T_{k+1}.
 constexpr int kHalfBytes = kTile * 128;  // 16 KB: 64 columns of 128 rows
 
-// Transpose of 16-byte chunks within each group of E consecutive lanes (E a
-// power of two): on entry chunk slot s of lane g + b (g the group's first lane)
-// holds chunk s of row b; on return slot s holds chunk b of row s.  One xor
-// step per bit swaps that bit between the lane and the slot index.
-template <int E>
-__device__ __forceinline__ void exchange_chunks(uint32_t (&u)[4 * E], int lane) {
-#pragma unroll
-  for (int m = E / 2; m >= 1; m >>= 1) {
-    const bool hi = (lane & m) != 0;
-#pragma unroll
-    for (int s0 = 0; s0 < E; ++s0) {
-      if (s0 & m) continue;
-      const int s1 = s0 | m;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // the lower lane keeps slot s0 and passes slot s1 up; the upper the reverse
-        const uint32_t send = hi ? u[4 * s0 + q] : u[4 * s1 + q];
-        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
-        u[4 * s0 + q] = hi ? recv : u[4 * s0 + q];
-        u[4 * s1 + q] = hi ? u[4 * s1 + q] : recv;
-      }
-    }
-  }
-}
-
 // (the two barriers of half 0's second piece exist at D = 128 only)
 template <int D>
 constexpr int num_bars() { return 20 + 2 * kItemRing + (D == 128 && kH0Pieces ? 2 : 0); }

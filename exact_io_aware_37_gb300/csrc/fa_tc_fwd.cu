@@ -385,22 +385,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           tc_fence_after();
           const bool row_ok = i < len;
           const float inv = l > 0.f ? 1.f / l : 0.f;
-          __nv_bfloat16* orow = p.o + (q.out_base + i) * D;
+          if constexpr (kDrop || D == 64) {
+            // row-per-lane stores: with dropout the exchange's registers would spill
+            // next to the keep words (and the generator bounds that forward anyway);
+            // at D = 64 the exchange's latency outweighs the store lines it saves
+            // (measured)
+            __nv_bfloat16* orow = p.o + (q.out_base + i) * D;
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c, o);
-            tmem_ld_wait(o);
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c);
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(t_o + c, o);
+              tmem_ld_wait(o);
+              if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4) {
-                uint4 u;
-                u.x = pack16x2<F16>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-                u.y = pack16x2<F16>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-                u.z = pack16x2<F16>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-                u.w = pack16x2<F16>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                dst[v4] = u;
+                for (int v4 = 0; v4 < 4; ++v4) {
+                  uint4 u;
+                  u.x = pack16x2<F16>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                  u.y = pack16x2<F16>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                  u.z = pack16x2<F16>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                  u.w = pack16x2<F16>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                  dst[v4] = u;
+                }
+              }
+            }
+          } else {
+            // 64 columns at a time: read out, normalised and packed by the row's own
+            // thread, then an 8 x 8 exchange of 16-byte chunks inside groups of eight
+            // lanes gives each store instruction four whole 128-byte row segments
+            // (one line each, instead of one line per lane)
+            const int grp = lane & ~7, sub = lane & 7;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 64) {
+              uint32_t pk[32];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t o[32];
+                tmem_ld32(t_o + c + 32 * h, o);
+                tmem_ld_wait(o);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  pk[16 * h + e] = pack16x2<F16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+              }
+              exchange_chunks<8>(pk, lane);
+              // slot s now holds chunk `sub` of row grp + s of this warp's 32
+#pragma unroll
+              for (int s8 = 0; s8 < 8; ++s8) {
+                const int row = qt * kBM + quad * 32 + grp + s8;
+                if (row < len)
+                  *reinterpret_cast<uint4*>(p.o + (q.out_base + row) * D + c + sub * 8) =
+                      make_uint4(pk[4 * s8], pk[4 * s8 + 1], pk[4 * s8 + 2], pk[4 * s8 + 3]);
               }
             }
           }

@@ -439,6 +439,32 @@ __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, 
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+
+// Transpose of 16-byte chunks within each group of E consecutive lanes (E a
+// power of two): on entry chunk slot s of lane g + b (g the group's first lane)
+// holds chunk s of row b; on return slot s holds chunk b of row s.  One xor
+// step per bit swaps that bit between the lane and the slot index.
+template <int E>
+__device__ __forceinline__ void exchange_chunks(uint32_t (&u)[4 * E], int lane) {
+#pragma unroll
+  for (int m = E / 2; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int s0 = 0; s0 < E; ++s0) {
+      if (s0 & m) continue;
+      const int s1 = s0 | m;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        // the lower lane keeps slot s0 and passes slot s1 up; the upper the reverse
+        const uint32_t send = hi ? u[4 * s0 + q] : u[4 * s1 + q];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        u[4 * s0 + q] = hi ? recv : u[4 * s0 + q];
+        u[4 * s1 + q] = hi ? u[4 * s1 + q] : recv;
+      }
+    }
+  }
+}
+
 // max(a, b, c)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
