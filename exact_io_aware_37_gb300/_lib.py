@@ -29,7 +29,7 @@ SIGNATURES = {
     "fa_selftest_wait_timeout": (_int, [_vp]),
     "fa_path_name": (_c.c_char_p, [_int, _int]),
     "fa_launch_count": (_c.c_ulonglong, []),
-    "fa_schedule_preview": (_int, [_int, _vp, _int, _int, _int, _int, _int, _vp, _vp, _int, _vp]),
+    "fa_schedule_preview": (_int, [_int, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _int, _vp]),
     "fa_last_error_detail": (_c.c_char_p, []),
     "fa_bwd_time_main_kernel": (None, [_vp, _vp]),
     "fa_fwd_dropout": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _f, _int, _vp, _int, _int, _f,

@@ -210,15 +210,17 @@ const char* fa_path_name(fa_dtype dt, int D) {
 
 unsigned long long fa_launch_count(void) { return g_launches.load(); }
 
-int fa_schedule_preview(int kernel, const int32_t* cu_seqlens, int B, int H, int N, int causal, int n_ctas,
+int fa_schedule_preview(int kernel, const int32_t* cu_seqlens, int B, int H, int N, int D, int causal, int n_ctas,
                         int* off, unsigned int* items, int cap, int* form) {
-  if ((kernel != 0 && kernel != 1) || B <= 0 || H <= 0 || N <= 0 || (causal != 0 && causal != 1) || n_ctas <= 0 ||
-      off == nullptr || form == nullptr || cap < 0 || (items == nullptr && cap > 0))
+  if ((kernel != 0 && kernel != 1) || B <= 0 || H <= 0 || N <= 0 || (D != 64 && D != 128) ||
+      (causal != 0 && causal != 1) || n_ctas <= 0 || off == nullptr || form == nullptr || cap < 0 ||
+      (items == nullptr && cap > 0))
     return -1;
   fa::Problem p{};
   p.B = B;
   p.H = H;
   p.N = N;
+  p.D = D;
   p.causal = causal;
   p.cu = cu_seqlens;  // only its presence matters to the schedule; the host copy is read below
   p.T = cu_seqlens ? cu_seqlens[B] : 0;

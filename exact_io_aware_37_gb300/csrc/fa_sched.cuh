@@ -35,6 +35,13 @@ namespace fa {
 
 constexpr int kSchedTile = 128;  // rows of a query tile and keys of a key tile
 
+// A host table groups heads only so that the operands the items of the heads
+// in flight re-read stay in L2; when those operands of all heads together take
+// at most this many bytes (well inside the 129 MB L2), the table is one group:
+// heaviest items first across all heads, which the least-loaded assignment
+// balances best.
+constexpr long long kSchedL2GroupBytes = 48ll << 20;
+
 // 32-bit arithmetic throughout (a 64-bit division is a called routine on the
 // GPU, which costs the register-starved roles a stack frame): the host only
 // builds closed-form lists of at most kMaxVirtualItems virtual items.

@@ -984,10 +984,13 @@ bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
   sc.n_virtual = (uint32_t)n;
   const int ctas = (int)std::min<long long>(n, std::min(ctas_max, kMaxSchedCtas));
   // Items in the order the grid used: with the mask, heavy-first inside
-  // balanced groups of kBwdHeadGroup heads (the order of grouped_heavy_first).
+  // balanced groups of kBwdHeadGroup heads (the order of grouped_heavy_first),
+  // or of all heads when their Q, dO and dQ accumulators fit in L2 together.
   std::vector<uint32_t> order((size_t)n);
   std::vector<int> weight((size_t)n);
-  const long long n_groups = (n_bh + kBwdHeadGroup - 1) / kBwdHeadGroup;
+  const long long head_bytes = 8ll * p.N * p.D;  // Q, dO (16-bit) and the float32 dQ accumulator
+  const long long group_heads = n_bh * head_bytes <= kSchedL2GroupBytes ? n_bh : (long long)kBwdHeadGroup;
+  const long long n_groups = (n_bh + group_heads - 1) / group_heads;
   const long long per = (n_bh + n_groups - 1) / n_groups;
   for (long long f = 0; f < n; ++f) {
     long long bh, kt;

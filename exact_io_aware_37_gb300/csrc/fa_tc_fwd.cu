@@ -664,10 +664,13 @@ bool fill_fwd_sched(const Problem& p, int ctas_max, FwdSched& sc) {
   sc.n_virtual = (uint32_t)n;
   const int ctas = (int)std::min<long long>(n, std::min(ctas_max, kMaxSchedCtas));
   // Pairs in the order the grid used: with the mask, heaviest first inside
-  // balanced groups of kFwdHeadGroup heads (the order of grouped_heavy_first).
+  // balanced groups of kFwdHeadGroup heads (the order of grouped_heavy_first),
+  // or of all heads when their K and V fit in L2 together.
   std::vector<uint32_t> order((size_t)n);
   std::vector<int> weight((size_t)n);
-  const long long n_groups = (n_bh + kFwdHeadGroup - 1) / kFwdHeadGroup;
+  const long long head_bytes = 4ll * p.N * p.D;  // K and V (16-bit)
+  const long long group_heads = n_bh * head_bytes <= kSchedL2GroupBytes ? n_bh : (long long)kFwdHeadGroup;
+  const long long n_groups = (n_bh + group_heads - 1) / group_heads;
   const long long per = (n_bh + n_groups - 1) / n_groups;
   for (long long f = 0; f < n; ++f) {
     long long bh, pair;

@@ -247,13 +247,16 @@ unsigned long long fa_launch_count(void);
 /*
  * Host-only view of the work lists of the persistent tensor-core launches
  * (instrumentation and tests; no GPU needed).  kernel 0 = the forward, whose
- * items are pairs of 128-row query tiles; kernel 1 = the D = 128 backward,
- * whose items are 128-key tiles.  cu_seqlens: NULL for dense input, else a
- * HOST copy of the packed offsets (int32[B+1]).  Two forms (written to
+ * items are pairs of 128-row query tiles; kernel 1 = the backward, whose
+ * items are 128-key tiles.  D: the head width, 64 or 128.  cu_seqlens: NULL
+ * for dense input, else a HOST copy of the packed offsets (int32[B+1]).  Two
+ * forms (written to
  * *form): 0 = a table worked out on the host, for dense inputs of at most
  * 4096 items -- items in the order the one-CTA-per-item grid would hand them
- * out (heaviest first inside groups of heads), each to the CTA with the least
- * work so far, at most min(n_ctas, 160) CTAs; 1 = the forward's closed-form
+ * out (heaviest first inside groups of heads -- one group of all heads when
+ * the operands they re-read fit in L2 together, which depends on the head
+ * width D), each to the CTA with the least work so far, at most
+ * min(n_ctas, 160) CTAs; 1 = the forward's closed-form
  * list, for larger or packed inputs -- unit u = b * H + h, the units' items
  * rank-major (all units' heaviest first), CTA c of n = min(n_ctas,
  * B * H * ranks) taking virtual item k * n + c for even k and
@@ -268,7 +271,7 @@ unsigned long long fa_launch_count(void);
  * items[off[i] .. off[i + 1]), in that order) and returns the number of
  * items; -1 for arguments out of range, -2 if `cap` is below the item count.
  */
-int fa_schedule_preview(int kernel, const int32_t* cu_seqlens, int B, int H, int N, int causal, int n_ctas,
+int fa_schedule_preview(int kernel, const int32_t* cu_seqlens, int B, int H, int N, int D, int causal, int n_ctas,
                         int* off, unsigned int* items, int cap, int* form);
 
 /* Attention dropout (tensortonic.com "FlashAttention" section 7: the backward
