@@ -36,6 +36,9 @@ DENSE_CASES = [
     (3, 6, 384, 128),
     (5, 7, 300, 64),
     (6, 3, 520, 128),
+    # many heads of one ragged tile each: 2048 and 256 tiny items in the host table
+    (64, 32, 40, 64),
+    (16, 16, 96, 128),
 ]
 
 
