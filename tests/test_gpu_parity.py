@@ -101,6 +101,25 @@ def test_packed_16bit(D, causal, dtype):
             f"packed {dtype} D={D} causal={causal}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_many_short_packed_sequences(D):
+    """200 packed sequences of 0-150 tokens: hundreds of (sequence, head) units
+    in the forward's closed-form list and the backward's queue, many of them
+    empty or one ragged tile, ranks a sequence lacks skipped."""
+    g = torch.Generator().manual_seed(4242 + D)
+    lengths = torch.randint(0, 151, (200,), generator=g).tolist()
+    lengths[:3] = [0, 1, 150]
+    cu = synth.cu_seqlens(lengths)
+    q, k, v, do = synth.qkv_do((4, int(cu[-1]), D), torch.bfloat16, seed_offset=40)
+    scale = default_scale(D)
+    got = run(q, k, v, do, True, scale, cu=cu, max_seqlen=max(lengths))
+    qn, kn, vn, don = (x.double().numpy() for x in (q, k, v, do))
+    O, L = oracle.forward_varlen(qn, kn, vn, cu, scale, True)
+    dQ, dK, dV, _ = oracle.backward_varlen(qn, kn, vn, don, cu, scale, True)
+    compare(torch.bfloat16, {n: f64(t) for n, t in got.items()}, dict(o=O, lse=L, dq=dQ, dk=dK, dv=dV),
+            f"200 short packed sequences D={D}")
+
+
 def test_causal_rows_ignore_future_keys():
     """Changing keys/values after row i leaves causal rows <= i unchanged
     (bit-identical: the kernel never reads them for those rows)."""
