@@ -237,40 +237,81 @@ def cpu_oracle_sample(q, k, v, do, scale, causal, budget_s=12.0, max_heads=None)
 
 
 def run_reference(args, rank):
-    """The oracle as the reference arm: each step is the oracle's forward +
-    backward on one head of the workload, on the host cores."""
+    """The oracle as the reference arm, on the host cores: each step is the
+    oracle's forward + backward on a bounded sample of the workload -- one
+    (b, h) head (train and the other dense configurations), one (sequence,
+    head) of the packed workload in turn, or, for the 32768-token window (whose
+    n x n head would take 8.6 GB a matrix), 256 query rows of a head at the end
+    of the sequence, forward and dQ rows, counted by the FLOPs they take."""
     if rank != 0:
         return
     from exact_io_aware_37_gb300 import synth
-    cfg = synth.WORKLOADS[WORKLOAD]
-    q, k, v, do = synth.make_dense(cfg)
-    B, H, N, D = q.shape
-    scale = 1.0 / D ** 0.5
     import oracle
-    qn, kn, vn, don = (x[0, 0].double().numpy() for x in (q, k, v, do))
-    for _ in range(args.warmup):
-        oracle.forward_head(qn, kn, vn, scale, CAUSAL)
-        oracle.backward_head(qn, kn, vn, don, scale, CAUSAL)
-    times = []
+    wl = "train" if args.workload == "train" else args.workload
+    if wl == "decode":
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times fwd+bwd workloads only"}))
+        return
+    name, causal = (WORKLOAD, CAUSAL) if wl == "train" else CONFIG_WORKLOADS[wl]
+    cfg = synth.WORKLOADS[name]
+    samples = []  # (q, k, v, do) of one sample as float64 arrays, and its FLOPs
+    if "n_seqs" in cfg:
+        q, k, v, do, cu, lengths = synth.make_varlen(cfg)
+        D = q.shape[-1]
+        for s, n in enumerate(lengths):
+            if n > 0:
+                a0, a1 = int(cu[s]), int(cu[s + 1])
+                samples.append((tuple(x[s % q.shape[0], a0:a1].double().numpy() for x in (q, k, v, do)),
+                                3.5 * flops_fwd(1, 1, int(n), D, causal)))
+        shape = dict(H=q.shape[0], T=int(cu[-1]), D=D, n_seqs=len(lengths))
+        sample = "one (sequence, head) of the packed workload per step, float64 numpy fwd+bwd"
+        rows = None
+    else:
+        q, k, v, do = synth.make_dense(cfg)
+        B, H, N, D = q.shape
+        shape = dict(B=B, H=H, N=N, D=D)
+        rows = np.arange(N - 256, N) if N > 8192 else None
+        for b in range(B):
+            for h in range(H):
+                arrs = tuple(x[b, h].double().numpy() for x in (q, k, v, do))
+                if rows is None:
+                    samples.append((arrs, 3.5 * flops_fwd(1, 1, N, D, causal)))
+                else:  # forward rows 4 D n_i + dQ rows 6 D n_i flops (scores recomputed)
+                    keys = (rows + 1) if causal else np.full(len(rows), N)
+                    samples.append((arrs, 10.0 * D * float(keys.sum())))
+        sample = ("one (b,h) head per step, float64 numpy fwd+bwd" if rows is None else
+                  "256 query rows at the end of one head per step: forward rows and dQ rows (float64 numpy), "
+                  "counted by the FLOPs they take")
+    scale = 1.0 / D ** 0.5
+
+    def one(arrs):
+        qn, kn, vn, don = arrs
+        if rows is None:
+            oracle.forward_head(qn, kn, vn, scale, causal)
+            oracle.backward_head(qn, kn, vn, don, scale, causal)
+        else:
+            oracle.forward_rows(qn, kn, vn, rows, scale, causal)
+            oracle.backward_dq_rows(qn, kn, vn, don, rows, scale, causal)
+
+    for w in range(args.warmup):
+        one(samples[w % len(samples)][0])
+    times, flops = [], 0.0
     for s in range(args.steps):
-        b, h = divmod(s % (B * H), H)
-        qn, kn, vn, don = (x[b, h].double().numpy() for x in (q, k, v, do))
+        arrs, f = samples[s % len(samples)]
         t0 = time.perf_counter()
-        oracle.forward_head(qn, kn, vn, scale, CAUSAL)
-        oracle.backward_head(qn, kn, vn, don, scale, CAUSAL)
+        one(arrs)
         times.append(time.perf_counter() - t0)
+        flops += f
     total = sum(times)
-    flops = 3.5 * flops_fwd(1, 1, N, D, CAUSAL) * args.steps
     value = flops / total / 1e12
     cores = os.cpu_count()
+    label = f"{name} {'causal' if causal else 'non-causal'}"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD} causal (one head per step)", "B": 1, "H": 1, "N": N, "D": D,
-                   "causal": CAUSAL},
+        "config": dict({"workload": f"{label} (one sample per step)", "causal": causal}, **shape),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"one (b,h) head of {WORKLOAD} per step, float64 numpy fwd+bwd"},
+                         "sample": f"{sample}; {label}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
