@@ -18,7 +18,7 @@ import torch
 from ._lib import FA_BF16, FA_F16, FA_F32, FAError, lib, library_path  # noqa: F401
 
 __all__ = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_get_last_device_error", "fa_strerror",
-           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
+           "fa_set_wait_limit_ns", "fa_selftest_wait_timeout", "fa_selftest_tile", "fa_path_name", "fa_launch_count", "fa_bwd_static_ws", "fa_bwd_time_main_kernel", "forward", "backward",
            "fa_decode", "fa_decode_workspace_size", "decode", "fa_fwd_dropout", "fa_bwd_dropout",
            "fa_bwd_deterministic", "fa_probe_ex2_rate", "FAError"]
 
@@ -103,6 +103,21 @@ def fa_get_last_device_error(stream=None):
 
 def fa_selftest_wait_timeout(stream=None):
     return lib().fa_selftest_wait_timeout(_stream(stream))
+
+
+def fa_selftest_tile(a, b, s_out, o_out, a_copy, stream=None):
+    """One-tile check of the tensor-core building blocks: s_out = a b^T,
+    o_out = round(s_out) b (float32), a_copy = a read back from its swizzled
+    shared-memory tile.  a, b, a_copy: [128, D] bf16 or fp16; returns the
+    status code."""
+    for t in (a, b, s_out, o_out, a_copy):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("fa_selftest_tile wants contiguous CUDA tensors")
+    if s_out.dtype != torch.float32 or o_out.dtype != torch.float32 or a_copy.dtype != a.dtype:
+        raise ValueError("s_out and o_out must be float32, a_copy of a's dtype")
+    dt = _DT.get(a.dtype, FA_F32)
+    return lib().fa_selftest_tile(_ptr(a), _ptr(b), _ptr(s_out), _ptr(o_out), _ptr(a_copy), a.shape[-1], dt,
+                                  _stream(stream))
 
 
 def fa_fwd(q, k, v, o, lse, causal, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):

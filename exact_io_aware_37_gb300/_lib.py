@@ -27,6 +27,7 @@ SIGNATURES = {
     "fa_get_last_device_error": (_int, [_vp]),
     "fa_set_wait_limit_ns": (None, [_c.c_ulonglong]),
     "fa_selftest_wait_timeout": (_int, [_vp]),
+    "fa_selftest_tile": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _int, _vp]),
     "fa_path_name": (_c.c_char_p, [_int, _int]),
     "fa_launch_count": (_c.c_ulonglong, []),
     "fa_schedule_preview": (_int, [_int, _vp, _int, _int, _int, _int, _int, _int, _vp, _vp, _int, _vp]),

@@ -22,7 +22,7 @@ LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
 SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_tc_fwd.cu", "fa_tc_bwd.cu", "fa_tc_bwd128.cu", "fa_static_ws.cu",
-           "fa_decode.cu", "fa_tc_bwd_dq.cu", "fa_probe.cu"]
+           "fa_decode.cu", "fa_tc_bwd_dq.cu", "fa_probe.cu", "fa_selftest.cu"]
 
 # The tensor-core kernels move registers between warpgroups with setmaxnreg
 # (384-thread kernels from 168 registers per thread at launch: the forward

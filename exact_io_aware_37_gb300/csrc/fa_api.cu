@@ -261,6 +261,22 @@ fa_status fa_selftest_wait_timeout(void* stream) {
   return fa_get_last_device_error(stream);
 }
 
+fa_status fa_selftest_tile(const void* a, const void* b, float* s_out, float* o_out, void* a_copy, int D,
+                           fa_dtype dtype, void* stream) {
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_BF16 && dtype != FA_F16) return FA_ERR_UNSUPPORTED;
+  fa_status st;
+  for (const void* p : {a, b, (const void*)s_out, (const void*)o_out, (const void*)a_copy})
+    if ((st = check_tensor(p)) != FA_OK) return st;
+  unsigned* word = nullptr;
+  g_detail[0] = 0;
+  if (note_error("status word", status_word(&word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_tile_selftest(a, b, D, dtype == FA_F16, s_out, o_out, a_copy, word, g_wait_limit_ns.load(),
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return fa_get_last_device_error(stream);
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int D, const int32_t* cu, int T, fa_dtype dt) {
   if (B < 0 || H < 0 || N < 0 || D <= 0 || (cu && T < 0)) return 0;
   const long long rows = row_count(B, H, N, cu, T);

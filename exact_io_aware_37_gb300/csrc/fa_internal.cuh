@@ -150,6 +150,9 @@ cudaError_t launch_simt_fwd(const Problem& p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_simt_bwd(const Problem& p, fa_dtype dt, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const Problem& p, fa_dtype dt, bool zero_dq_acc, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, cudaStream_t s);
+// One-tile check of the tensor-core building blocks (fa_selftest.cu); D in {64, 128}.
+cudaError_t launch_tile_selftest(const void* a, const void* b, int D, bool f16, float* s_out, float* o_out,
+                                 void* a_copy, unsigned* status, unsigned long long limit_ns, cudaStream_t s);
 
 // tensor-core path (bf16, D in {64, 128})
 cudaError_t launch_tc_fwd(const Problem& p, cudaStream_t s);

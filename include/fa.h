@@ -202,6 +202,27 @@ void fa_set_wait_limit_ns(unsigned long long limit_ns);
 fa_status fa_selftest_wait_timeout(void* stream);
 
 /*
+ * Unit check of the tensor-core building blocks on one tile, for tests: the
+ * products the method is made of (tensortonic.com "FlashAttention", section
+ * 5: scores S = Q K^T of a query tile against a key tile, then the weights of
+ * that tile times its values) formed the way the kernels form them.  One CTA
+ * loads a and b with TMA, forms S = a b^T in tensor memory, writes it to
+ * s_out, rounds it to dtype and forms O = round(S) b with tensor-memory
+ * operand A, writes O to o_out, and copies a back out of its swizzled
+ * shared-memory tile into a_copy.
+ *   a, b     in : DEVICE [128, D] row-major, dtype (FA_BF16 or FA_F16)
+ *   s_out    out: DEVICE float32 [128, 128]
+ *   o_out    out: DEVICE float32 [128, D]
+ *   a_copy   out: DEVICE [128, D], dtype; equals a bit for bit when correct
+ *   D        64 or 128 (FA_ERR_UNSUPPORTED otherwise, or for FA_F32)
+ * Every pointer must be non-NULL (FA_ERR_INVALID) and 16-byte aligned
+ * (FA_ERR_ALIGN).  Synchronises `stream` and returns
+ * fa_get_last_device_error(stream); FA_ERR_CUDA if a launch fails.
+ */
+fa_status fa_selftest_tile(const void* a, const void* b, float* s_out, float* o_out, void* a_copy, int D,
+                           fa_dtype dtype, void* stream);
+
+/*
  * Name of the kernel family fa_fwd / fa_bwd launch for this dtype and head
  * width ("tcgen05" for bf16, "simt_f32" for float32), or NULL when
  * unsupported.  Host only.

@@ -105,6 +105,19 @@ def test_backward_argument_validation(lib):
     assert det == INVALID
 
 
+def test_tile_selftest_argument_validation(lib):
+    def tile(a=0x1000, b=0x1000, s=0x1000, o=0x1000, ac=0x1000, D=128, dt=0):
+        return lib.fa_selftest_tile(a, b, s, o, ac, D, dt, None)
+    assert tile(D=96) == UNSUPPORTED
+    assert tile(D=32) == UNSUPPORTED
+    assert tile(dt=1) == UNSUPPORTED     # float32 has no tensor-core tile
+    assert tile(dt=7) == UNSUPPORTED
+    assert tile(a=None) == INVALID
+    assert tile(ac=None) == INVALID
+    assert tile(s=0x1004) == ALIGN
+    assert tile(o=0x1008) == ALIGN
+
+
 def test_workspace_size(lib):
     f = lib.fa_bwd_workspace_size
     # D vector (4 B per row) + float32 dQ accumulator + a 256-byte block for the
