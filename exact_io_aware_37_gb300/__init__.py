@@ -115,9 +115,12 @@ def fa_selftest_tile(a, b, s_out, o_out, a_copy, stream=None):
             raise ValueError("fa_selftest_tile wants contiguous CUDA tensors")
     if s_out.dtype != torch.float32 or o_out.dtype != torch.float32 or a_copy.dtype != a.dtype:
         raise ValueError("s_out and o_out must be float32, a_copy of a's dtype")
+    D = a.shape[-1]
+    if (a.dim() != 2 or tuple(a.shape) != (128, D) or b.shape != a.shape or a_copy.shape != a.shape
+            or b.dtype != a.dtype or tuple(s_out.shape) != (128, 128) or tuple(o_out.shape) != (128, D)):
+        raise ValueError("fa_selftest_tile wants a, b, a_copy [128, D], s_out [128, 128], o_out [128, D]")
     dt = _DT.get(a.dtype, FA_F32)
-    return lib().fa_selftest_tile(_ptr(a), _ptr(b), _ptr(s_out), _ptr(o_out), _ptr(a_copy), a.shape[-1], dt,
-                                  _stream(stream))
+    return lib().fa_selftest_tile(_ptr(a), _ptr(b), _ptr(s_out), _ptr(o_out), _ptr(a_copy), D, dt, _stream(stream))
 
 
 def fa_fwd(q, k, v, o, lse, causal, scale=None, cu_seqlens=None, max_seqlen=None, stream=None):
