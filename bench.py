@@ -7,6 +7,14 @@ JSON line (rank 0).  ``value`` is fwd+bwd TFLOP/s with FLOPs counted as
 4*B*H*N^2*D (halved when causal) for the forward pass and 2.5x that for the
 backward pass; ``fwd_tflops`` is the forward pass alone.
 
+The step is first run eagerly (one host launch per kernel), with CUDA events
+between the passes and around the main backward kernel: that loop gives the
+forward / backward split and the roofline of the dominant kernel, and goes
+under ``eager``.  The same step is then captured once in a CUDA graph and
+replayed ``steps`` times; the replays (the same kernels and work, without the
+host launch path between them) give ``value`` and ``ms_per_step``.  If the
+capture fails the eager loop gives them.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun each rank runs its own replica (the path has no exchange
@@ -210,6 +218,59 @@ def max_over_ranks(dist, x, device):
 def barrier(dist):
     if dist is not None:
         dist.barrier()
+
+
+def graph_replay_measure(step, flops, steps, warmup, device, dist, world, local, unit="TFLOP/s"):
+    """The step captured once in a CUDA graph and replayed: the library's calls
+    enqueue no host synchronisation and no allocation, so the step's kernels
+    (the same launches, the same work) replay without the host launch path
+    between them.  `step(stream)` enqueues one step on `stream`.  Times `steps`
+    replays with CUDA events on the replay stream, barrier and synchronize on
+    both sides, max over ranks, clocks sampled meanwhile; returns a dict for
+    the JSON line ("unavailable" and the reason if the capture fails)."""
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(torch.cuda.current_stream(device))
+        for _ in range(max(warmup, 3)):
+            g.replay()
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream(device)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clocks:
+            barrier(dist)
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            barrier(dist)
+        ms = max_over_ranks(dist, t0.elapsed_time(t1), device) / steps
+        del g
+        per_s = 1e12 if unit == "TFLOP/s" else 1e9  # flops: FLOPs, or bytes for GB/s
+        return {"value": world * flops / (ms * 1e-3) / per_s, "unit": unit, "ms_per_step": ms,
+                "launch": "the step's kernels replayed from one CUDA graph", "clocks": clocks.summary()}
+    except Exception as e:  # reported, not fatal: the eager measurement stands on its own
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
+def headline_from_graph(line, graph, launches, world, peak_tf):
+    """Make the graph-replayed step the line's headline when it was measured:
+    value, ms_per_step and clocks come from the replays, the eager loop's go
+    under "eager"; the replays launch the same kernels per step as the eager
+    loop, whose count the library took."""
+    eager = {"value": line["value"], "ms_per_step": line["ms_per_step"], "clocks": line["clocks"],
+             "launch": "one host launch per kernel"}
+    if "value" not in graph:
+        line["graph_replay"] = graph
+        return
+    line["value"], line["ms_per_step"], line["clocks"] = graph["value"], graph["ms_per_step"], graph["clocks"]
+    line["config"]["launch"] = "CUDA graph replay of the whole step (its calls captured once)"
+    line["gpu_launches"] = launches
+    if peak_tf is not None:
+        line["fwdbwd_frac_of_peak"] = graph["value"] / world / peak_tf
+    line["eager"] = eager
 
 
 def kernel_source_sha(path):
@@ -458,6 +519,11 @@ def main():
 
     if not args.no_e2e:
         line["e2e"] = e2e_measure(fa, q_h, k_h, v_h, do_h, scale, device, stream, dist, world, args)
+    graph = graph_replay_measure(
+        lambda st: (fwd_call(q, k, v, o, lse, scale, st), bwd_call(q, k, v, o, lse, do, dq, dk, dv, scale, ws, st)),
+        f_step, args.steps, args.warmup, device, dist, world, local)
+    assert fa.fa_get_last_device_error() == 0
+    headline_from_graph(line, graph, launches, world, peak_tf)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, heads, secs = cpu_oracle_sample(q_h, k_h, v_h, do_h, scale, CAUSAL)
@@ -538,11 +604,17 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
     ws = torch.empty(fa.fa_bwd_workspace_size(q, cu, max_seqlen), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
+    def fwd_on(st):
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, cu, max_seqlen, stream=st)
+
+    def bwd_on(st):
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, cu, max_seqlen, workspace=ws, stream=st)
+
     def fwd():
-        fa.fa_fwd(q, k, v, o, lse, causal, scale, cu, max_seqlen, stream=stream)
+        fwd_on(stream)
 
     def bwd():
-        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, cu, max_seqlen, workspace=ws, stream=stream)
+        bwd_on(stream)
 
     for _ in range(args.warmup):
         fwd()
@@ -572,6 +644,9 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
         barrier(dist)
     launches = fa.fa_launch_count() - launches0
     assert fa.fa_get_last_device_error() == 0
+    graph = graph_replay_measure(lambda st: (fwd_on(st), bwd_on(st)), 3.5 * f_fwd, args.steps,
+                                 args.warmup, device, dist, world, local)
+    assert fa.fa_get_last_device_error() == 0
     ms_step = max_over_ranks(dist, t0.elapsed_time(t1), device) / args.steps
     ms_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     ms_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
@@ -600,6 +675,7 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
                      "peak_kind": f"bf16 dense burst, {peak_kind}"},
         "gpu_launches": launches, "clocks": clocks.summary(),
     }
+    headline_from_graph(line, graph, launches, world, peak_tf)
     print(json.dumps(line), flush=True)
 
 
@@ -642,6 +718,9 @@ def bench_decode(fa, synth, args, dist, rank, world, local, device):
     ms = max_over_ranks(dist, a.elapsed_time(b), device) / args.steps
     elem = q.element_size()
     step_bytes = (2 * B * H * nk * D + 2 * B * H * nq * D) * elem + B * H * nq * 4
+    graph = graph_replay_measure(lambda st: fa.fa_decode(q, k, v, o, lse, True, scale, workspace=ws, stream=st),
+                                 step_bytes, args.steps, args.warmup, device, dist, world, local, unit="GB/s")
+    assert fa.fa_get_last_device_error() == 0
     gbs = world * step_bytes / (ms * 1e-3) / 1e9
     peak_gbs, peak_kind = hbm_peak()
 
@@ -695,6 +774,7 @@ def bench_decode(fa, synth, args, dist, rank, world, local, device):
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
     }
+    headline_from_graph(line, graph, launches, world, None)
     print(json.dumps(line), flush=True)
 
 
