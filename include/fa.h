@@ -49,6 +49,17 @@
  * out) are latched in a per-device status word read by
  * fa_get_last_device_error.
  *
+ * CUDA graphs: fa_fwd, fa_bwd, fa_fwd_dropout, fa_bwd_dropout,
+ * fa_bwd_deterministic and fa_decode enqueue no host synchronisation and no
+ * allocation, and pass their work lists by value in the kernel parameters, so
+ * a stream capture of them replays correctly on new contents of the same
+ * buffers.  Make one eager call of each first: it performs the one-time
+ * per-device look-ups (status word address, tensor-map encoder).  A captured
+ * backward reuses its workspace on every replay (its tile counter is reset by
+ * the replay itself); replays that overlap on the GPU need workspaces of their
+ * own, as overlapping eager calls do.  Dropout replays the captured seed and
+ * offset.
+ *
  * Errors: invalid arguments return an error code before anything is launched;
  * nothing aborts the process.
  */
