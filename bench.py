@@ -51,6 +51,9 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 TRAFFIC_BY_SOURCE = {
     # tc_bwd128_kernel<128, bf16>, B2 H32 N4096 D128 causal: 405.0 MB read + 220.6 MB written
     "ce594b4f7f1d737c9d87a65e888f7f6a4c6bfdfd89f587f781844eb3c667351c": 625.6e6,
+    # the same file with only its host code changed (the cached schedule's key
+    # also holds the head width); the kernel's device code is as captured
+    "4a6f022408ced7574c15298975ae7ebd1f8b8b42f797497503f9dd5c947c92e8": 625.6e6,
     # decode_split_kernel, B16 H32 nq1 nk8192 D128: 2147.7 MB read + 3.8 MB written
     "fee09d5aa4225f18dc40dd1517d297a22d708da1eb55e0890c30901cdf5a3bb5": 2151.5e6,
 }

@@ -1033,18 +1033,18 @@ bool fill_bwd_sched(const Problem& p, int ctas_max, BwdSched& sc) {
 bool build_sched(const Problem& p, BwdSched& sc) {
   const int ctas = sm_count();
   static std::mutex mu;
-  static long long key[5] = {-1, -1, -1, -1, -1};
+  static long long key[6] = {-1, -1, -1, -1, -1, -1};
   static BwdSched cached;
-  const long long want[5] = {p.B, p.H, p.N, p.causal, ctas};
+  const long long want[6] = {p.B, p.H, p.N, p.D, p.causal, ctas};  // the table's head groups depend on D
   if (p.cu != nullptr) return fill_bwd_sched(p, ctas, sc);  // closed form: nothing to cache
   std::lock_guard<std::mutex> lock(mu);
-  if (std::equal(want, want + 5, key)) {
+  if (std::equal(want, want + 6, key)) {
     sc = cached;
     return true;
   }
   if (!fill_bwd_sched(p, ctas, sc)) return false;
   cached = sc;
-  std::copy(want, want + 5, key);
+  std::copy(want, want + 6, key);
   return true;
 }
 
