@@ -147,8 +147,8 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, causal, scale=None, cu_seqlens=Non
     _check(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens)
     B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    need = fa_bwd_workspace_size(q, cu_seqlens, max_seqlen)
     if workspace is None:
+        need = fa_bwd_workspace_size(q, cu_seqlens, max_seqlen)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = lib().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                       B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T, _DT[q.dtype],
@@ -204,8 +204,8 @@ def fa_bwd_dropout(q, k, v, o, lse, dout, dq, dk, dv, causal, p_drop, seed, offs
     _check(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens)
     B, H, N, D, T = _dims(q, cu_seqlens, max_seqlen)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    need = fa_bwd_workspace_size(q, cu_seqlens, max_seqlen)
     if workspace is None:
+        need = fa_bwd_workspace_size(q, cu_seqlens, max_seqlen)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = lib().fa_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                               B, H, N, D, scale, int(bool(causal)), _ptr(cu_seqlens), T, _DT[q.dtype], float(p_drop),
