@@ -80,7 +80,7 @@ def hbm_peak():
 
 class ClockSampler:
     """SM clock, power and clock-event reasons sampled while the timed region
-    runs: read in-process through NVML (read-only queries, every ~1 ms, so a
+    runs: read in-process through NVML (read-only queries, every ~0.2 ms, so a
     timed region of a few milliseconds still gets many samples); nvidia-smi
     at 50 ms where the NVML library cannot be loaded."""
 
