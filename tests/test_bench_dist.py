@@ -1,6 +1,7 @@
-"""bench.py's multi-process plumbing on the CPU (gloo, world size 2): the
+"""bench.py on the CPU: the multi-process plumbing (gloo, world size 2) -- the
 barrier and the max-over-ranks timing the replicas use, and the reference
-arm doing its work on rank 0 only."""
+arm doing its work on rank 0 only -- and how the graph-replayed step becomes
+the headline, or, when it cannot be captured, leaves the eager one standing."""
 
 import multiprocessing as mp
 import os
@@ -64,3 +65,28 @@ def test_reference_arm_prints_one_contract_line():
     assert d["warmup"] >= 3 and d["steps"] == 1 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_graph_replay_headline_and_fallback():
+    """The graph-replayed step becomes the headline with the eager loop kept
+    beside it; when the capture fails (here: no GPU) the eager line stands and
+    says why."""
+    sys.path.insert(0, ROOT)
+    import bench
+    eager_clocks = {"sm_mhz": 2070.0, "samples": 3}
+    line = {"value": 100.0, "ms_per_step": 2.0, "clocks": eager_clocks, "config": {"workload": "w"},
+            "gpu_launches": 8, "fwdbwd_frac_of_peak": 0.05}
+    graph = {"value": 125.0, "unit": "TFLOP/s", "ms_per_step": 1.6, "launch": "graph",
+             "clocks": {"sm_mhz": 2070.0, "samples": 9}}
+    bench.headline_from_graph(line, graph, 8, 1, 2000.0)
+    assert line["value"] == 125.0 and line["ms_per_step"] == 1.6 and line["clocks"]["samples"] == 9
+    assert line["eager"]["value"] == 100.0 and line["eager"]["ms_per_step"] == 2.0
+    assert line["eager"]["clocks"] is eager_clocks
+    assert line["fwdbwd_frac_of_peak"] == 125.0 / 2000.0 and line["gpu_launches"] == 8
+    assert "graph" in line["config"]["launch"].lower()
+
+    failed = bench.graph_replay_measure(lambda st: None, 1e12, 2, 1, torch.device("cpu"), None, 1, 0)
+    assert set(failed) == {"unavailable"}
+    line2 = {"value": 100.0, "ms_per_step": 2.0, "clocks": eager_clocks, "config": {"workload": "w"}}
+    bench.headline_from_graph(line2, failed, 8, 1, 2000.0)
+    assert line2["value"] == 100.0 and "eager" not in line2 and line2["graph_replay"] == failed
