@@ -13,7 +13,11 @@ forward / backward split and the roofline of the dominant kernel, and goes
 under ``eager``.  The same step is then captured once in a CUDA graph and
 replayed ``steps`` times; the replays (the same kernels and work, without the
 host launch path between them) give ``value`` and ``ms_per_step``.  If the
-capture fails the eager loop gives them.
+capture fails the eager loop gives them.  After the headline's timed regions
+the default run also measures the other configurations (mid, long non-causal,
+packed, long window) for a few steps each and carries their figures under
+``workloads`` (``--no-workloads`` leaves them out; ``--workload NAME`` gives
+one configuration's full line).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -389,6 +393,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="train workload only: leave out the short measurements of the other configurations")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="16-bit input type (the same synthetic draws, rounded to it)")
     ap.add_argument("--dropout", type=float, default=0.0,
@@ -533,6 +539,17 @@ def main():
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{heads} of {B * H} (b,h) heads of {WORKLOAD} causal, float64 "
                                           f"numpy fwd+bwd, {secs:.1f} s"}
+    if not args.no_workloads and args.dtype == "bf16" and args.dropout == 0 and not args.deterministic:
+        # the other configurations, each fwd+bwd on device-resident inputs (a
+        # short eager loop, then the step replayed from a CUDA graph), after
+        # the headline's timed regions so their heat does not reach it
+        wl_steps = max(10, min(args.steps, 30))
+        summaries = {}
+        for w in WORKLOADS_IN_DEFAULT_RUN:
+            wl = config_line(fa, synth, args, w, wl_steps, dist, rank, world, local, device)
+            if wl is not None:
+                summaries[w] = workload_summary(wl)
+        line["workloads"] = summaries
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(dist)
@@ -570,6 +587,8 @@ def probe_ex2(fa, synth, local, device):
 
 
 # The other configurations: synth workload name and whether the mask is on.
+# Carried by the default run's line under "workloads" (each a short measurement).
+WORKLOADS_IN_DEFAULT_RUN = ("mid", "long_nc", "varlen", "window")
 CONFIG_WORKLOADS = {
     "mid": ("mid_b4h16n1024d64", True),
     "long": ("long_b2h32n4096d128", True),
@@ -580,12 +599,33 @@ CONFIG_WORKLOADS = {
 
 
 def bench_config(fa, synth, args, dist, rank, world, local, device):
+    """Print the line of the configuration --workload names."""
+    line = config_line(fa, synth, args, args.workload, args.steps, dist, rank, world, local, device)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+def workload_summary(line):
+    """The figures of a configuration's line that the default run carries."""
+    keep = ("value", "unit", "ms_per_step", "fwd_tflops", "bwd_tflops", "fwd_frac_of_peak", "fwdbwd_frac_of_peak",
+            "ms_bwd_main_kernel", "steps")
+    out = {k: line[k] for k in keep if k in line}
+    out["workload"] = line["config"]["workload"]
+    out["launch"] = line["config"].get("launch", "eager")
+    out["eager_value"] = line.get("eager", {}).get("value", line["value"])
+    out["roofline_frac"] = line["roofline"]["frac"]
+    out["clocks"] = {k: line["clocks"].get(k) for k in ("sm_mhz", "sm_min_mhz", "reasons", "samples")}
+    return out
+
+
+def config_line(fa, synth, args, workload, steps, dist, rank, world, local, device):
     """fwd+bwd TFLOP/s of one configuration with inputs resident on the
     device: fa_fwd then fa_bwd per step, each timed with CUDA events on the
     launching stream, the main backward kernel timed alone by the events the
-    library records around it.  Packed input counts sum_s 4 H n_s^2 D (half
-    with the mask) forward FLOPs."""
-    name, causal = CONFIG_WORKLOADS[args.workload]
+    library records around it, then the step replayed from a CUDA graph.
+    Packed input counts sum_s 4 H n_s^2 D (half with the mask) forward FLOPs.
+    Every rank measures; rank 0 gets the line, the others None."""
+    name, causal = CONFIG_WORKLOADS[workload]
     cfg = dict(synth.WORKLOADS[name], dtype=args.dtype)
     cu = max_seqlen = None
     if "n_seqs" in cfg:
@@ -624,7 +664,7 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
         bwd()
     torch.cuda.synchronize()
     assert fa.fa_get_last_device_error() == 0
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     for e in ev:
         e[3].record(stream)
         e[4].record(stream)
@@ -635,7 +675,7 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
         torch.cuda.synchronize()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for st in range(args.steps):
+        for st in range(steps):
             ev[st][0].record(stream)
             fwd()
             ev[st][1].record(stream)
@@ -647,10 +687,10 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
         barrier(dist)
     launches = fa.fa_launch_count() - launches0
     assert fa.fa_get_last_device_error() == 0
-    graph = graph_replay_measure(lambda st: (fwd_on(st), bwd_on(st)), 3.5 * f_fwd, args.steps,
+    graph = graph_replay_measure(lambda st: (fwd_on(st), bwd_on(st)), 3.5 * f_fwd, steps,
                                  args.warmup, device, dist, world, local)
     assert fa.fa_get_last_device_error() == 0
-    ms_step = max_over_ranks(dist, t0.elapsed_time(t1), device) / args.steps
+    ms_step = max_over_ranks(dist, t0.elapsed_time(t1), device) / steps
     ms_fwd = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     ms_bwd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     ms_main = statistics.mean(e[3].elapsed_time(e[4]) for e in ev)
@@ -659,11 +699,11 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
     bwd_main_tf = 2.5 * f_fwd / (ms_main * 1e-3) / 1e12
     kernel = f"tc_bwd128_kernel<{D}>"
     if rank != 0:
-        return
+        return None
     line = {
         "metric": f"attention fwd & fwd+bwd TFLOP/s ({args.dtype}, {'causal' if causal else 'non-causal'}) "
                   "and % of GB300 BF16 tensor peak",
-        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": args.dtype, "data": "synthetic",
         "config": dict({"workload": f"{name} {'causal' if causal else 'non-causal'}", "causal": causal,
@@ -679,7 +719,7 @@ def bench_config(fa, synth, args, dist, rank, world, local, device):
         "gpu_launches": launches, "clocks": clocks.summary(),
     }
     headline_from_graph(line, graph, launches, world, peak_tf)
-    print(json.dumps(line), flush=True)
+    return line
 
 
 DECODE_WORKLOAD = "decode_b16h32q1k8192d128"

@@ -90,3 +90,18 @@ def test_graph_replay_headline_and_fallback():
     line2 = {"value": 100.0, "ms_per_step": 2.0, "clocks": eager_clocks, "config": {"workload": "w"}}
     bench.headline_from_graph(line2, failed, 8, 1, 2000.0)
     assert line2["value"] == 100.0 and "eager" not in line2 and line2["graph_replay"] == failed
+
+
+def test_workload_summary_keeps_the_headline_figures():
+    sys.path.insert(0, ROOT)
+    import bench
+    line = {"value": 385.0, "unit": "TFLOP/s", "ms_per_step": 0.078, "fwd_tflops": 320.0, "bwd_tflops": 318.0,
+            "fwd_frac_of_peak": 0.17, "fwdbwd_frac_of_peak": 0.2, "ms_bwd_main_kernel": 0.05, "steps": 20,
+            "config": {"workload": "mid_b4h16n1024d64 causal", "launch": "graph"},
+            "eager": {"value": 315.0}, "roofline": {"frac": 0.22},
+            "clocks": {"sm_mhz": 2070.0, "sm_min_mhz": 2002.0, "reasons": [], "samples": 4, "power_w_max": 1.0}}
+    s = bench.workload_summary(line)
+    assert s["value"] == 385.0 and s["eager_value"] == 315.0 and s["roofline_frac"] == 0.22
+    assert s["workload"] == "mid_b4h16n1024d64 causal" and s["launch"] == "graph"
+    assert s["clocks"] == {"sm_mhz": 2070.0, "sm_min_mhz": 2002.0, "reasons": [], "samples": 4}
+    assert set(bench.WORKLOADS_IN_DEFAULT_RUN) <= set(bench.CONFIG_WORKLOADS)
