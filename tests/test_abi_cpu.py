@@ -324,6 +324,20 @@ def test_table_groups_heads_only_beyond_l2(lib, kernel):
     assert firsts[group] % r != heaviest(4096)   # the group's next-heaviest items come before other heads
 
 
+@pytest.mark.parametrize("kernel,N", [(0, 2048), (1, 1024)])
+def test_table_depends_on_the_head_width(lib, kernel, N):
+    """At B4 H16 the operands the items re-read fit in L2 together at D = 64
+    but not at D = 128 (forward at N = 2048: K, V 32 MB / 64 MB; backward at
+    N = 1024: Q, dO, dQ accumulator 32 MB / 64 MB), so the two head widths get
+    different tables for the same B, H, N and mask: a table cached on the host
+    has to be keyed by D as well."""
+    a = _preview(lib, kernel, 4, 16, N, 1, 152, D=64)
+    b = _preview(lib, kernel, 4, 16, N, 1, 152, D=128)
+    assert a[3] == 0 and b[3] == 0
+    assert sorted(a[2]) == sorted(b[2])          # the same items...
+    assert (a[1], a[2]) != (b[1], b[2])          # ...handed out differently
+
+
 @pytest.mark.parametrize("kernel,B,H,N,causal", [
     (0, 1, 64, 32768, 1),     # 8192 pairs
     (0, 3, 40, 12345, 1)])    # ragged length
