@@ -421,3 +421,34 @@ def test_persistent_schedule_refusals(lib):
     assert _preview(lib, 1, 2, 32, 4096, 1, 152, cap=4)[0] == -2
     assert _preview(lib, 1, 1, 32, 32768, 1, 152, cap=100)[0] == -2
     assert _preview(lib, 0, 1, 64, 32768, 1, 152, cap=100)[0] == -2
+
+
+# Host calls that allocate device or pinned memory, or wait for the device.
+_ALLOC_OR_SYNC = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cudaHostAlloc|cudaMallocHost|cudaDeviceSynchronize|"
+                            r"cudaStreamSynchronize|cudaEventSynchronize|cudaMemcpy|cudaMemset|cudaMemcpyToSymbol|"
+                            r"cudaMemcpyFromSymbol)\s*\(")
+
+
+def _strip_comments(src):
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.sub(r"//[^\n]*", "", src)
+
+
+def test_compute_calls_neither_allocate_nor_wait():
+    """The attention and decoding entry points only enqueue work on the
+    caller's stream (which is what lets a caller capture them in a CUDA
+    graph): no translation unit calls an allocator or a waiting or
+    synchronous copy call, except the status read-back
+    (fa_get_last_device_error, which the self-tests return) and the ex2 rate
+    probe, both documented as synchronising."""
+    csrc = os.path.join(ROOT, "exact_io_aware_37_gb300", "csrc")
+    allowed = {"fa_api.cu": 3, "fa_probe.cu": 2}
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh")):
+            continue
+        hits = _ALLOC_OR_SYNC.findall(_strip_comments(open(os.path.join(csrc, name)).read()))
+        assert len(hits) == allowed.get(name, 0), (name, hits)
+    api = _strip_comments(open(os.path.join(csrc, "fa_api.cu")).read())
+    body = api[api.index("fa_status fa_get_last_device_error("):]
+    body = body[:body.index("\n}\n")]
+    assert len(_ALLOC_OR_SYNC.findall(body)) == 3       # all three sit in the status read-back
