@@ -14,8 +14,8 @@ under ``eager``.  The same step is then captured once in a CUDA graph and
 replayed ``steps`` times; the replays (the same kernels and work, without the
 host launch path between them) give ``value`` and ``ms_per_step``.  If the
 capture fails the eager loop gives them.  After the headline's timed regions
-the default run also measures the other configurations (mid, long non-causal,
-packed, long window) for a few steps each and carries their figures under
+the default run on one GPU also measures the other configurations (mid, long
+non-causal, packed, long window) for a few steps each and carries their figures under
 ``workloads`` (``--no-workloads`` leaves them out; ``--workload NAME`` gives
 one configuration's full line).
 
@@ -539,7 +539,8 @@ def main():
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{heads} of {B * H} (b,h) heads of {WORKLOAD} causal, float64 "
                                           f"numpy fwd+bwd, {secs:.1f} s"}
-    if not args.no_workloads and args.dtype == "bf16" and args.dropout == 0 and not args.deterministic:
+    if (not args.no_workloads and world == 1 and args.dtype == "bf16" and args.dropout == 0
+            and not args.deterministic):
         # the other configurations, each fwd+bwd on device-resident inputs (a
         # short eager loop, then the step replayed from a CUDA graph), after
         # the headline's timed regions so their heat does not reach it
