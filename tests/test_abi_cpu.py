@@ -452,3 +452,46 @@ def test_compute_calls_neither_allocate_nor_wait():
     body = api[api.index("fa_status fa_get_last_device_error("):]
     body = body[:body.index("\n}\n")]
     assert len(_ALLOC_OR_SYNC.findall(body)) == 3       # all three sit in the status read-back
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fa.h"
+
+int main(void) {
+  /* argument checks return before any CUDA call, so this runs without a GPU */
+  if (fa_fwd((void*)0, (void*)0, (void*)0, (void*)0, (float*)0, 1, 1, 128, 128, 0.125f, 1, NULL, 0, FA_BF16,
+             NULL) != FA_ERR_INVALID) return 1;
+  if (fa_fwd((void*)0x1000, (void*)0x1000, (void*)0x1000, (void*)0x1000, (float*)0x1000, 1, 1, 128, 96, 0.125f, 0,
+             NULL, 0, FA_BF16, NULL) != FA_ERR_UNSUPPORTED) return 2;
+  if (fa_bwd_workspace_size(2, 32, 4096, 128, NULL, 0, FA_BF16) !=
+      (size_t)2 * 32 * 4096 * 4 + (size_t)2 * 32 * 4096 * 128 * 4 + 256) return 3;
+  if (strcmp(fa_strerror(FA_ERR_ALIGN), "tensor pointer not 16-byte aligned") != 0) return 4;
+  if (fa_path_name(FA_BF16, 128) == NULL || fa_path_name(FA_BF16, 96) != NULL) return 5;
+  if (FA_BWD_STATIC_WS_BYTES != (size_t)16 << 20) return 6;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    """A C99 caller that includes include/fa.h, links libfa_gb300.so and calls
+    the host-side parts of the boundary: the header needs no C++ and the
+    library no Python."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(fa_build.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-L", libdir, "-lfa_gb300", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
